@@ -1,0 +1,368 @@
+#!/usr/bin/env python3
+"""Benchmark: ring-chunked attention forward TFLOP/s on GB300.
+
+One step = one ra_fwd launch over the whole headline workload (GQA causal:
+B=2, H=32, Hkv=8, S=16384, D=128, P=8 chunks of 2048), inputs resident in
+HBM.  FLOPs are counted exactly: 4*B*H*D*N_pairs with N_pairs = S(S+1)/2
+(allowed query/key pairs; masked work the kernel still does on diagonal
+tiles is not counted; softmax work is not counted).
+
+L2 is flushed (a 256 MiB write) between timed steps; each step is timed with
+CUDA events on the stream the kernel is launched on.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica of
+the workload (nothing is exchanged), so scaling is weak and the value is the
+sum over ranks' FLOPs divided by the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded row sample of the
+same workload (the CPU baseline) with the same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ring_chunked_attention_gb300.inputs import HEADLINE, WORKLOADS, make_inputs, sample_rows  # noqa: E402
+
+METRIC = "ring-chunked attention fwd TFLOP/s at 1 GB300; % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["ring_chunked_attention_gb300/csrc/ra_fwd.cu",
+                  "ring_chunked_attention_gb300/csrc/ra_ptx.cuh",
+                  "ring_chunked_attention_gb300/csrc/ra_api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_for(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_sha") != kernel_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, power, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------- CPU oracle arm
+def cpu_oracle_sample(w, budget_s: float = 15.0, seed: int = 0, inputs=None):
+    """Time the fp64 oracle (as it stands) on a bounded deterministic row
+    sample of workload ``w``; return (TFLOP/s, threads, description)."""
+    import numpy as np
+
+    import oracle
+
+    q, k, v = inputs if inputs is not None else make_inputs(w)
+    threads = oracle.default_threads()
+    rows = sample_rows(w, n_random=256, every=w.S // 4, seed=seed).numpy()
+    rng = np.random.default_rng(seed)
+    rows = rng.permutation(rows)
+    # calibrate on a small batch, then size the sample to the budget
+    s_of = rows % w.S
+
+    def flops(rs):
+        s = rs % w.S
+        keys = (s + 1) if w.causal else np.full_like(s, w.S)
+        return float(4 * w.D * keys.sum())
+
+    n0 = min(len(rows), max(threads * 4, 64))
+    t0 = time.perf_counter()
+    oracle.attn_direct(q, k, v, w.causal, w.scale, rows=rows[:n0], threads=threads)
+    dt0 = time.perf_counter() - t0
+    rate = flops(rows[:n0]) / max(dt0, 1e-6)
+    # grow the sample until it carries about budget_s of work
+    cum = np.cumsum(4 * w.D * (((s_of + 1) if w.causal else np.full_like(s_of, w.S))).astype(np.float64))
+    n = int(np.searchsorted(cum, rate * budget_s)) + 1
+    n = max(n0, min(n, len(rows)))
+    sample = rows[:n]
+    t0 = time.perf_counter()
+    oracle.attn_direct(q, k, v, w.causal, w.scale, rows=sample, threads=threads)
+    dt = time.perf_counter() - t0
+    tflops = flops(sample) / dt / 1e12
+    desc = (f"{n} query rows (chunk boundaries, every {w.S // 4}th row and seeded random rows "
+            f"of every (b,h)) of {w.name}, fp64 two-pass, {dt:.1f} s")
+    return tflops, threads, desc, dt
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    steps = []
+    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    inputs = make_inputs(w)
+    tf, threads, desc = None, None, None
+    for i in range(args.warmup + args.steps):
+        tf_i, threads, desc, dt = cpu_oracle_sample(w, budget_s=budget, seed=i, inputs=inputs)
+        if i >= args.warmup:
+            steps.append((tf_i, dt))
+    tf = statistics.mean(s[0] for s in steps)
+    ms = statistics.mean(s[1] for s in steps) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv,
+                                            "S": w.S, "D": w.D, "P": w.P, "causal": w.causal},
+            "cpu_baseline": {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": tf, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+
+    import ring_chunked_attention_gb300 as ra
+    from ring_chunked_attention_gb300 import build as rab
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+    if rank == 0:
+        rab.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    rab.build()  # no-op once built; fails loudly if the toolchain is missing
+
+    w = WORKLOADS[args.workload]
+    q, k, v = make_inputs(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    out = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ra.ra_fwd(qd, kd, vd, P=w.P, causal=w.causal, scale=w.scale, out=out, lse=lse,
+                  stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    st = ra.ra_get_last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {ra.ra_status_string(st)}")
+
+    sampler = ClockSampler(dev)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for e0, e1 in evs:
+        flush.fill_(1.0)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    kernel_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    if ra.ra_get_last_device_status() != 0:
+        raise RuntimeError("device status reported a timeout in the timed region")
+    ms = statistics.mean(kernel_ms)
+
+    # end to end through the public call with host buffers (pinned), copies timed
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    outh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    lseh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2
+    d2h = outh.numel() * 2 + lseh.numel() * 4
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(e2e_steps + 1)]
+    for i, (e0, e1) in enumerate(e2e_evs):
+        flush.fill_(1.0)
+        e0.record(stream)
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        outh.copy_(out, non_blocking=True)
+        lseh.copy_(lse, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in e2e_evs[1:])
+
+    # slowest rank decides
+    if ws > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms, e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+
+    flops = w.flops
+    value = ws * flops / (ms * 1e-3) / 1e12
+    e2e_value = ws * flops / (e2e_ms * 1e-3) / 1e12
+    per_launch_tflops = flops / (ms * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    traffic = traffic_for(w.name)
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            tf, threads, desc, _ = cpu_oracle_sample(w, budget_s=args.cpu_seconds, inputs=(q, k, v))
+            cpu = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "S": w.S, "D": w.D,
+                       "P": w.P, "causal": w.causal, "flops_per_step": flops,
+                       "l2": "flushed between timed steps (256 MiB write)",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": "tensor", "achieved": per_launch_tflops, "peak": peak,
+                         "unit": UNIT, "frac": per_launch_tflops / peak,
+                         "peak_source": f"{src} bf16 dense burst",
+                         "frac_of_sustained": per_launch_tflops / float(peaks["bf16_tflops_sustained"]),
+                         "traffic": traffic},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms),
+                          "max": max(kernel_ms)},
+            "kernel_sha": kernel_sha(),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,131 @@
+/*
+ * ringattn.h -- C ABI of libringattn: single-GPU ring-chunked attention
+ * forward for NVIDIA GB300 (sm_103a).
+ *
+ * The method is the compute side of the "Ring Attention" fused kernel of the
+ * mKernel overview page (chatgpz.de, German translation of the MarkTechPost
+ * article), table "Die fünf verschmolzenen Kerne", row Ring Attention: the key
+ * and value sequence is cut into blocks that rotate around a ring; the local
+ * FlashAttention step consumes the block received before, folding it into a
+ * running (max, sum, accumulator) triple, while the next block is being moved.
+ * Here the P blocks ("chunks") all live in this GPU's memory: "moving the next
+ * block" is the TMA staging of the next key/value tiles into shared memory
+ * while the tensor cores consume the current ones.  Nothing crosses a GPU
+ * boundary.
+ *
+ * Conventions shared by every call:
+ *   - Every pointer to tensor data is a DEVICE pointer into memory the caller
+ *     owns; the library never allocates, frees or retains caller memory.  The
+ *     only library-owned device state is one status word per device (see
+ *     ra_get_last_device_status) and the kernels' code.
+ *   - Every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and returns without waiting; results are valid once the
+ *     stream has reached the work.
+ *   - Arguments are validated on the host before anything is launched; on any
+ *     error nothing is launched and the outputs are untouched.
+ *   - bf16 means IEEE-754 binary16-brain (1 sign, 8 exponent, 7 mantissa bits).
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ra_status {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, H % Hkv != 0, S % P != 0,
+                             non-finite scale, n < 1 */
+  RA_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle: D not 64/128,
+                             S/P not a multiple of 128, pointer not 16-byte aligned,
+                             negative scale, device is not sm_103, sizes past 2^31 rows */
+  RA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute query,
+                             tensor-map encode); ra_last_cuda_error() gives the code */
+  RA_ERR_TIMEOUT = 4      /* a bounded wait inside a kernel gave up (reported by
+                             ra_get_last_device_status) */
+} ra_status;
+
+/*
+ * ra_fwd -- ring-chunked attention forward.
+ *
+ * Computes, for batch b, query head h, query row s (all rows, all heads):
+ *     g      = h / (H / Hkv)                        (grouped-query attention)
+ *     x_t    = scale * <q[b,s,h,:], k[b,t,g,:]>      for allowed keys t
+ *              (allowed: all t when causal == 0; t <= s when causal != 0)
+ *     out[b,s,h,:] = sum_t softmax_t(x) * v[b,t,g,:]          (bf16, RNE)
+ *     lse[b,h,s]   = ln sum_t exp(x_t)                        (fp32)
+ * The keys are cut into P equal contiguous chunks of C = S/P rows.  A query
+ * row in chunk i folds chunk i first (its own), then i-1, i-2, ... (the block
+ * its ring predecessor would send), wrapping around for non-causal attention;
+ * causal chunks j > i hold no allowed key and are skipped.  Each chunk is
+ * folded with the online-softmax update (FlashAttention), so the result is
+ * exact softmax attention up to floating-point rounding.
+ *
+ *   q    [B, S, H,   D] bf16, contiguous (row-major, D fastest)
+ *   k, v [B, S, Hkv, D] bf16, contiguous
+ *   out  [B, S, H,   D] bf16, contiguous, written
+ *   lse  [B, H, S]      fp32, contiguous, written; may be NULL (not written)
+ *   B, H, Hkv, S, D, P > 0;  H % Hkv == 0;  S % P == 0
+ *   supported: D in {64, 128};  (S / P) % 128 == 0;  scale >= 0 and finite
+ *   (scale == 0 is legal and gives uniform weights over the allowed keys)
+ *   q, k, v, out 16-byte aligned; lse 4-byte aligned.
+ *   out must not overlap q, k or v.
+ * Returns RA_OK once the kernel is enqueued.  A kernel that had to give up a
+ * bounded internal wait leaves out/lse partly written and records
+ * RA_ERR_TIMEOUT for ra_get_last_device_status.
+ */
+ra_status ra_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+                 int Hkv, int S, int D, int P, int causal, float scale, void* stream);
+
+/*
+ * ra_merge_partials -- combine n normalised partial attention results that
+ * were computed over disjoint key sets (for instance one per ring chunk) into
+ * the result over their union: the online-softmax fold of the same page's
+ * Ring Attention row, written in log-sum-exp form.
+ *
+ *   o_parts   [n, B, S, H, D]  bf16 (o_is_fp32 == 0) or fp32 (o_is_fp32 != 0);
+ *             partial k holds O_k = (sum over its keys of e^{x_t} v_t) /
+ *             (sum over its keys of e^{x_t}), as ra_fwd writes it
+ *   lse_parts [n, B, H, S]     fp32; lse_k = ln(sum over its keys of e^{x_t});
+ *             -inf marks a partial with no key, which contributes nothing
+ *   out       [B, S, H, D]     bf16, written: sum_k e^{lse_k - lse} O_k
+ *   lse       [B, H, S]        fp32, written: ln sum_k e^{lse_k}; may be NULL
+ *   When every lse_k of a row is -inf the row gets out = 0 and lse = -inf.
+ *   n >= 1; B, H, S, D > 0; D % 8 == 0; o_parts and out 16-byte aligned.
+ */
+ra_status ra_merge_partials(const void* o_parts, int o_is_fp32, const float* lse_parts, int n,
+                            void* out, float* lse, int B, int H, int S, int D, void* stream);
+
+/*
+ * ra_get_last_device_status -- synchronise `stream`, then read and clear this
+ * device's sticky status word.  Returns RA_ERR_TIMEOUT if any kernel launched
+ * since the previous query gave up a bounded wait (its outputs are then not
+ * valid), RA_ERR_CUDA if the synchronisation itself failed, else RA_OK.
+ */
+ra_status ra_get_last_device_status(void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ra_status_string(ra_status s);
+
+/* The cudaError_t value behind the most recent RA_ERR_CUDA on this thread. */
+int ra_last_cuda_error(void);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+int ra_version(void);
+
+/*
+ * Test hook for the failure path: when `timeout_ns` > 0, subsequent ra_fwd
+ * launches on this process use that wait limit instead of the default (2 s);
+ * when `skip_value_load` != 0 the producer deliberately never issues the
+ * first value-tile copy, so the consumer's bounded wait must run out and the
+ * launch must report RA_ERR_TIMEOUT.  Pass (0, 0) to restore normal launches.
+ */
+void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
+
+/* Drop cached tensor maps and device queries (no device memory is held). */
+void ra_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RINGATTN_H */

@@ -1,0 +1,177 @@
+"""ring_chunked_attention_gb300 -- Python binding of libringattn.
+
+The compute path is the C ABI in ``include/ringattn.h`` (CUDA kernels for
+sm_103a).  This module only marshals arguments: it takes torch tensors for
+device memory and streams, checks shapes/dtypes, and passes raw pointers to
+the library.  There is no fallback: if ``libringattn.so`` is missing or
+cannot be loaded, every call raises.
+
+Functions carry the C names:
+
+* :func:`ra_fwd` -- ring-chunked attention forward (out, lse);
+* :func:`ra_merge_partials` -- merge normalised partials over disjoint key sets;
+* :func:`ra_get_last_device_status`, :func:`ra_status_string`,
+  :func:`ra_debug_set_fault`, :func:`ra_shutdown`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = ["ra_fwd", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+           "ra_debug_set_fault", "ra_shutdown", "ra_version", "RaError", "library_path",
+           "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT"]
+
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libringattn.so")
+_lib = None
+
+EXPORTS = ("ra_fwd", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+           "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_shutdown")
+
+
+class RaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {ra_status_string(code)}"
+                         + (f" (cudaError {_load().ra_last_cuda_error()})" if code == RA_ERR_CUDA else ""))
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"libringattn.so is not built ({_LIB_PATH}); run "
+                           "`python -m ring_chunked_attention_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.ra_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.ra_fwd.restype = i
+    lib.ra_merge_partials.argtypes = [vp, i, vp, i, vp, vp, i, i, i, i, vp]
+    lib.ra_merge_partials.restype = i
+    lib.ra_get_last_device_status.argtypes = [vp]
+    lib.ra_get_last_device_status.restype = i
+    lib.ra_status_string.argtypes = [i]
+    lib.ra_status_string.restype = ctypes.c_char_p
+    lib.ra_last_cuda_error.argtypes = []
+    lib.ra_last_cuda_error.restype = i
+    lib.ra_version.argtypes = []
+    lib.ra_version.restype = i
+    lib.ra_debug_set_fault.argtypes = [ctypes.c_longlong, i]
+    lib.ra_debug_set_fault.restype = None
+    lib.ra_shutdown.argtypes = []
+    lib.ra_shutdown.restype = None
+    _lib = lib
+    return lib
+
+
+def _stream_ptr(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(code: int, what: str):
+    if code != RA_OK:
+        raise RaError(code, what)
+
+
+def ra_status_string(code: int) -> str:
+    return _load().ra_status_string(int(code)).decode()
+
+
+def ra_version() -> int:
+    return int(_load().ra_version())
+
+
+def ra_fwd(q, k, v, *, P: int, causal: bool, scale: float | None = None, out=None, lse=None,
+           want_lse: bool = True, stream=None):
+    """Ring-chunked attention forward.  ``q`` [B,S,H,D], ``k``/``v``
+    [B,S,Hkv,D] bf16 CUDA tensors (contiguous).  Returns ``(out, lse)`` with
+    ``out`` [B,S,H,D] bf16 and ``lse`` [B,H,S] fp32 (``None`` when
+    ``want_lse`` is false and no ``lse`` buffer is given).  ``scale``
+    defaults to 1/sqrt(D)."""
+    import torch
+
+    lib = _load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{n} must be a contiguous 4-D bf16 CUDA tensor")
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != (B, S, Hkv, D):
+        raise ValueError("k and v must be [B,S,Hkv,D] matching q")
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S)
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous [B,H,S] fp32 tensor")
+    if tuple(out.shape) != (B, S, H, D) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B,S,H,D] bf16 tensor")
+    code = lib.ra_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                      None if lse is None else lse.data_ptr(), B, H, Hkv, S, D, int(P),
+                      int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(code, "ra_fwd")
+    return out, lse
+
+
+def ra_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_ptr: int | None, B: int,
+               H: int, Hkv: int, S: int, D: int, P: int, causal: bool, scale: float,
+               stream=None) -> int:
+    """The C call with plain integers (device addresses); returns the status code."""
+    return int(_load().ra_fwd(q_ptr, k_ptr, v_ptr, out_ptr, lse_ptr, B, H, Hkv, S, D, P,
+                              int(bool(causal)), float(scale), _stream_ptr(stream)))
+
+
+def ra_merge_partials(o_parts, lse_parts, *, out=None, lse=None, want_lse: bool = True,
+                      stream=None):
+    """Merge ``n`` normalised partials: ``o_parts`` [n,B,S,H,D] (bf16 or
+    fp32), ``lse_parts`` [n,B,H,S] fp32.  Returns ``(out, lse)``."""
+    import torch
+
+    lib = _load()
+    if o_parts.dim() != 5 or not o_parts.is_cuda or not o_parts.is_contiguous():
+        raise ValueError("o_parts must be a contiguous [n,B,S,H,D] CUDA tensor")
+    if o_parts.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("o_parts must be bf16 or fp32")
+    n, B, S, H, D = o_parts.shape
+    if (lse_parts.dtype != torch.float32 or tuple(lse_parts.shape) != (n, B, H, S)
+            or not lse_parts.is_contiguous()):
+        raise ValueError("lse_parts must be a contiguous [n,B,H,S] fp32 tensor")
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=o_parts.device)
+    code = lib.ra_merge_partials(o_parts.data_ptr(), int(o_parts.dtype == torch.float32),
+                                 lse_parts.data_ptr(), n, out.data_ptr(),
+                                 None if lse is None else lse.data_ptr(), B, H, S, D,
+                                 _stream_ptr(stream))
+    _check(code, "ra_merge_partials")
+    return out, lse
+
+
+def ra_get_last_device_status(stream=None) -> int:
+    """Synchronise ``stream``, read and clear the device status word; returns
+    the status code (``RA_OK`` or ``RA_ERR_TIMEOUT`` or ``RA_ERR_CUDA``)."""
+    return int(_load().ra_get_last_device_status(_stream_ptr(stream)))
+
+
+def ra_debug_set_fault(timeout_ns: int, skip_value_load: bool) -> None:
+    _load().ra_debug_set_fault(int(timeout_ns), int(bool(skip_value_load)))
+
+
+def ra_shutdown() -> None:
+    _load().ra_shutdown()

@@ -1,0 +1,272 @@
+// ra_api.cu -- the C ABI of libringattn: argument validation, tensor-map
+// encoding (cached), work decomposition and launch, status reporting.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "ra_internal.h"
+#include "ringattn.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+ra_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return RA_ERR_CUDA;
+}
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
+std::mutex g_mu;
+unsigned long long g_timeout_ns = kDefaultTimeoutNs;
+int g_skip_value_load = 0;
+
+// per-device facts, queried once
+struct DeviceInfo {
+  bool valid = false;
+  bool sm103 = false;
+  int sms = 0;
+  unsigned int* status = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+
+ra_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.valid) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    unsigned int* st = nullptr;
+    if ((e = ra::status_word_ptr(&st)) != cudaSuccess) return cuda_fail(e);
+    d.sm103 = (major == 10 && minor == 3);
+    d.sms = sms;
+    d.status = st;
+    d.valid = true;
+  }
+  *out = &d;
+  return RA_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+ra_status get_encoder(EncodeTiledFn* fn) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (q != cudaDriverEntryPointSuccess || !p) return cuda_fail(cudaErrorSymbolNotFound);
+    g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  *fn = g_encode;
+  return RA_OK;
+}
+
+// A [rows = B*S, heads, D] bf16 tensor read as 128-row x 64-column boxes,
+// 128-byte swizzled (the layout the tensor-core descriptors expect).
+struct MapKey {
+  const void* ptr;
+  long long rows;
+  int heads, D;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && heads == o.heads && D == o.D;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  unsigned long long stamp;
+  bool used;
+};
+constexpr int kMapCache = 32;
+MapEntry g_maps[kMapCache];
+unsigned long long g_stamp = 0;
+
+ra_status tensor_map(const void* ptr, long long rows, int heads, int D, CUtensorMap* out) {
+  const MapKey key{ptr, rows, heads, D};
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (auto& e : g_maps)
+      if (e.used && e.key == key) {
+        e.stamp = ++g_stamp;
+        *out = e.map;
+        return RA_OK;
+      }
+  }
+  EncodeTiledFn enc = nullptr;
+  ra_status st = get_encoder(&enc);
+  if (st != RA_OK) return st;
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof m);
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int victim = 0;
+  for (int i = 0; i < kMapCache; ++i) {
+    if (!g_maps[i].used) { victim = i; break; }
+    if (g_maps[i].stamp < g_maps[victim].stamp) victim = i;
+  }
+  g_maps[victim] = MapEntry{key, m, ++g_stamp, true};
+  *out = m;
+  return RA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+ra_status ra_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+                 int Hkv, int S, int D, int P, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || P <= 0) return RA_ERR_INVALID_ARG;
+  if (H % Hkv != 0 || S % P != 0) return RA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return RA_ERR_INVALID_ARG;
+  if (scale < 0.0f) return RA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
+  const int C = S / P;
+  if (C % 128 != 0) return RA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_UNSUPPORTED;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return RA_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * S;
+  if (rows >= (1ll << 31) || (long long)B * H * (S / 128) >= (1ll << 31))
+    return RA_ERR_UNSUPPORTED;
+
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  if (!dev->sm103) return RA_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tk, tv;
+  if ((st = tensor_map(q, rows, H, D, &tq)) != RA_OK) return st;
+  if ((st = tensor_map(k, rows, Hkv, D, &tk)) != RA_OK) return st;
+  if ((st = tensor_map(v, rows, Hkv, D, &tv)) != RA_OK) return st;
+
+  ra::FwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.out = out;
+  a.lse = lse;
+  a.status = dev->status;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.S = S;
+  a.P = P;
+  a.causal = causal ? 1 : 0;
+  a.tiles = S / 128;
+  a.tpc = C / 128;
+  const int G = H / Hkv;
+  if (G % 2 == 0) {
+    a.mode = ra::MODE_HEADS;
+    a.groups = B * Hkv * (G / 2);
+    a.nq = a.tiles;
+  } else if (a.tpc % 2 == 0) {
+    a.mode = ra::MODE_QTILES;
+    a.groups = B * H;
+    a.nq = a.tiles / 2;
+  } else {
+    a.mode = ra::MODE_SINGLE;
+    a.groups = B * H;
+    a.nq = a.tiles;
+  }
+  a.n_items = a.groups * a.nq;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    a.timeout_ns = g_timeout_ns;
+    a.skip_value_load = g_skip_value_load;
+  }
+  const int grid = a.n_items < dev->sms ? a.n_items : dev->sms;
+  cudaError_t e = ra::launch_fwd(D, tq, tk, tv, a, grid, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return RA_OK;
+}
+
+ra_status ra_merge_partials(const void* o_parts, int o_is_fp32, const float* lse_parts, int n,
+                            void* out, float* lse, int B, int H, int S, int D, void* stream) {
+  if (!o_parts || !lse_parts || !out) return RA_ERR_INVALID_ARG;
+  if (n < 1 || B <= 0 || H <= 0 || S <= 0 || D <= 0) return RA_ERR_INVALID_ARG;
+  if (D % 8 != 0) return RA_ERR_UNSUPPORTED;
+  if (!aligned16(o_parts) || !aligned16(out)) return RA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(lse_parts) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return RA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  if (!dev->sm103) return RA_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * S * H;
+  const long long units = rows * (D / 8);
+  long long grid = (units + 255) / 256;
+  const long long cap = (long long)dev->sms * 8;  // 8 resident 256-thread blocks per SM
+  if (grid > cap) grid = cap;
+  cudaError_t e = ra::launch_merge(o_parts, o_is_fp32, lse_parts, n, out, lse, rows, H, S, D,
+                                   (int)grid, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return RA_OK;
+}
+
+ra_status ra_get_last_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int v = 0;
+  e = ra::read_and_clear_status(&v);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return (v & ra::kStatusTimeout) ? RA_ERR_TIMEOUT : RA_OK;
+}
+
+const char* ra_status_string(ra_status s) {
+  switch (s) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_INVALID_ARG: return "RA_ERR_INVALID_ARG";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED";
+    case RA_ERR_CUDA: return "RA_ERR_CUDA";
+    case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT";
+  }
+  return "RA_ERR_UNKNOWN";
+}
+
+int ra_last_cuda_error(void) { return g_last_cuda_error; }
+
+int ra_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+void ra_debug_set_fault(long long timeout_ns, int skip_value_load) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_timeout_ns = timeout_ns > 0 ? (unsigned long long)timeout_ns : kDefaultTimeoutNs;
+  g_skip_value_load = skip_value_load ? 1 : 0;
+}
+
+void ra_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto& e : g_maps) e.used = false;
+  for (auto& d : g_dev) d = DeviceInfo{};
+  g_timeout_ns = kDefaultTimeoutNs;
+  g_skip_value_load = 0;
+}
+
+}  // extern "C"

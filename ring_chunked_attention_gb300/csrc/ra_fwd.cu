@@ -1,0 +1,571 @@
+// ra_fwd.cu -- persistent, warp-specialised ring-chunked attention forward
+// for sm_103a (tcgen05 tensor cores, tensor memory, TMA).
+//
+// Method: the "Ring Attention" row of the mKernel overview page (table "Die
+// fünf verschmolzenen Kerne"): the key/value sequence is consumed block by
+// block in ring order while the next block is being moved, and each block is
+// folded into the exact softmax result with the FlashAttention online-softmax
+// update.  On one GPU the "ring transfer" of the next block is the TMA
+// staging of the next key/value tiles into shared memory, which runs ahead of
+// the tensor cores across chunk boundaries without draining.
+//
+// CTA organisation (one CTA per SM, persistent over work items):
+//   warps 0-3  softmax + correction + epilogue for query slot 0 (TMEM lanes 0-127)
+//   warps 4-7  the same for query slot 1
+//   warp  8    TMA producer: Q tiles, then K/V tiles into an NS-stage ring
+//   warp  9    MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V
+// A work item is two 128-row query tiles sharing one key/value stream (two
+// heads of one GQA group, or two consecutive tiles of one head), so every
+// K/V tile staged in shared memory feeds two MMAs.
+//
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [  0,128) S_0   (P_0 as packed bf16 overwrites its first 64 columns)
+//   [128,256) S_1   (P_1 likewise)
+//   [256,256+D) O_0,  [256+D,256+2D) O_1
+//
+// Every wait is bounded: on timeout the CTA raises a shared abort flag, sets
+// the device status word, lets its in-flight copies and MMAs finish (bounded
+// too), frees tensor memory and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ra_internal.h"
+#include "ra_ptx.cuh"
+
+namespace ra {
+
+__device__ unsigned int g_status_word;
+
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per tile
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+
+template <int D>
+struct Layout {
+  static constexpr int DK = D / 64;                // 128-byte swizzle blocks per row
+  static constexpr int NS = (D == 128) ? 2 : 4;    // K/V ring depth
+  static constexpr int BLOCK = 128 * 128;          // one [128 rows x 64 cols] bf16 block
+  static constexpr int TILE = kBM * D * 2;         // one 128-row tile, all D
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + 2 * TILE;
+  static constexpr int V_OFF = K_OFF + NS * TILE;
+  static constexpr int BAR_OFF = V_OFF + NS * TILE;
+  // barrier indices
+  static constexpr int Q_FULL = 0, Q_EMPTY = 2, K_FULL = 4, K_EMPTY = 4 + NS, V_FULL = 4 + 2 * NS,
+                       V_EMPTY = 4 + 3 * NS, S_FULL = 4 + 4 * NS, P_FULL = 6 + 4 * NS,
+                       O_FREE = 8 + 4 * NS, DONE = 10 + 4 * NS, N_BARS = 11 + 4 * NS;
+  static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
+  static constexpr int BYTES = MISC_OFF + 16;
+  static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
+  static constexpr uint32_t S_COL(int i) { return 128u * i; }
+  static constexpr uint32_t O_COL(int i) { return 256u + (uint32_t)D * i; }
+};
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
+// B K-major (0) or MN-major (1), shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+struct Item {
+  int b, kvh;
+  int h[2];
+  int qt[2];
+  int valid1;
+};
+
+__device__ __forceinline__ Item decode_item(const FwdArgs& a, int x) {
+  const int qi = x / a.groups, g = x % a.groups;
+  const int q = a.causal ? (a.nq - 1 - qi) : qi;  // causal: heaviest rows first
+  const int G = a.H / a.Hkv;
+  Item it;
+  if (a.mode == MODE_HEADS) {
+    const int hp_per = G / 2;
+    it.b = g / (a.Hkv * hp_per);
+    const int r = g % (a.Hkv * hp_per);
+    it.kvh = r / hp_per;
+    it.h[0] = it.kvh * G + 2 * (r % hp_per);
+    it.h[1] = it.h[0] + 1;
+    it.qt[0] = it.qt[1] = q;
+    it.valid1 = 1;
+  } else {
+    it.b = g / a.H;
+    const int h = g % a.H;
+    it.kvh = h / G;
+    it.h[0] = it.h[1] = h;
+    if (a.mode == MODE_QTILES) {
+      it.qt[0] = 2 * q;
+      it.qt[1] = 2 * q + 1;
+      it.valid1 = 1;
+    } else {
+      it.qt[0] = it.qt[1] = q;
+      it.valid1 = 0;
+    }
+  }
+  return it;
+}
+
+// k-th item of this CTA: snake order over rounds of gridDim.x items, so that
+// heaviest-first causal work balances across CTAs.
+__device__ __forceinline__ int item_index(int k) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+__device__ __forceinline__ int qmax_of(const Item& it) {
+  return it.valid1 ? max(it.qt[0], it.qt[1]) : it.qt[0];
+}
+
+__device__ __forceinline__ int n_steps(const FwdArgs& a, const Item& it) {
+  return a.causal ? qmax_of(it) + 1 : a.tiles;
+}
+
+// Key tile visited at step u: chunks in ring order starting from the query
+// tiles' own chunk i (i, i-1, i-2, ... wrapping for non-causal); inside a
+// chunk the tiles ascend; causal stops the own chunk at the diagonal tile and
+// never visits chunks after i.
+__device__ __forceinline__ int step_tile(const FwdArgs& a, const Item& it, int u) {
+  const int ci = it.qt[0] / a.tpc;
+  if (a.causal) {
+    const int nd = qmax_of(it) - ci * a.tpc + 1;
+    if (u < nd) return ci * a.tpc + u;
+    u -= nd;
+    const int j = ci - 1 - u / a.tpc;
+    return j * a.tpc + u % a.tpc;
+  }
+  int j = ci - u / a.tpc;
+  if (j < 0) j += a.P;
+  return j * a.tpc + u % a.tpc;
+}
+
+__device__ __forceinline__ bool needs(const FwdArgs& a, const Item& it, int slot, int kt) {
+  if (slot == 1 && !it.valid1) return false;
+  return !a.causal || kt <= it.qt[slot];
+}
+
+// Bounded wait on one mbarrier phase (single thread).
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       unsigned long long timeout_ns, unsigned int* status) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        if (status) atomicOr(status, kStatusTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, const FwdArgs& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, a.timeout_ns, a.status);
+}
+
+// Bounded wait used while tearing down after an abort: never raises the flag
+// again and gives up after at most 100 ms.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long t) {
+  volatile int never = 0;
+  if (!mbar_try_wait(bar, parity))
+    wait_slow(bar, parity, &never, t < 100000000ull ? t : 100000000ull, nullptr);
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the warp follows its verdict.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          const FwdArgs& a) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, a) ? 1 : 0;
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// ----------------------------------------------------------------- producer
+template <int D>
+__device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                         const FwdArgs& a, uint32_t sbase, volatile int* abort_flag) {
+  using L = Layout<D>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const uint64_t pol_kv = l2_policy_evict_last();
+  const uint64_t pol_q = l2_policy_evict_first();
+  uint32_t q_cnt[2] = {0, 0};
+  uint32_t kv_cnt = 0;
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    if (k * (int)gridDim.x >= a.n_items) break;
+    const int x = item_index(k);
+    if (x >= a.n_items) continue;
+    const Item it = decode_item(a, x);
+#pragma unroll
+    for (int slot = 0; slot < 2 && ok; ++slot) {
+      if (slot == 1 && !it.valid1) continue;
+      if (q_cnt[slot] > 0 &&
+          !wait_bounded(bar(L::Q_EMPTY + slot), (q_cnt[slot] - 1) & 1, abort_flag, a)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(bar(L::Q_FULL + slot), L::TILE);
+      for (int kb = 0; kb < L::DK; ++kb)
+        tma_load_3d(sbase + L::Q_OFF + slot * L::TILE + kb * L::BLOCK, tq, bar(L::Q_FULL + slot),
+                    kb * 64, it.h[slot], it.b * a.S + it.qt[slot] * kBM, pol_q);
+      ++q_cnt[slot];
+    }
+    const int ns = n_steps(a, it);
+    for (int u = 0; u < ns && ok; ++u) {
+      const int kt = step_tile(a, it, u);
+      const int st = kv_cnt % L::NS;
+      const uint32_t ph = (kv_cnt / L::NS) & 1;
+      const int row = it.b * a.S + kt * kBN;
+      if (!wait_bounded(bar(L::K_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
+      mbar_arrive_expect_tx(bar(L::K_FULL + st), L::TILE);
+      for (int kb = 0; kb < L::DK; ++kb)
+        tma_load_3d(sbase + L::K_OFF + st * L::TILE + kb * L::BLOCK, tk, bar(L::K_FULL + st),
+                    kb * 64, it.kvh, row, pol_kv);
+      if (!wait_bounded(bar(L::V_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
+      mbar_arrive_expect_tx(bar(L::V_FULL + st), L::TILE);
+      if (!(a.skip_value_load && kv_cnt == 0))
+        for (int kb = 0; kb < L::DK; ++kb)
+          tma_load_3d(sbase + L::V_OFF + st * L::TILE + kb * L::BLOCK, tv, bar(L::V_FULL + st),
+                      kb * 64, it.kvh, row, pol_kv);
+      ++kv_cnt;
+    }
+  }
+  if (!ok) {
+    // Let every copy this thread issued land before shared memory goes away:
+    // wait (bounded) for the last armed phase of each full barrier.
+    for (int slot = 0; slot < 2; ++slot)
+      if (q_cnt[slot] > 0) wait_drain(bar(L::Q_FULL + slot), (q_cnt[slot] - 1) & 1, a.timeout_ns);
+    for (uint32_t c = (kv_cnt > (uint32_t)L::NS ? kv_cnt - L::NS : 0); c < kv_cnt; ++c) {
+      wait_drain(bar(L::K_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
+      wait_drain(bar(L::V_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- MMA issuer
+template <int D>
+__device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
+                         volatile int* abort_flag) {
+  using L = Layout<D>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  constexpr uint32_t idesc_s = make_idesc(kBM, kBN, 0);
+  constexpr uint32_t idesc_pv = make_idesc(kBM, D, 1);
+  uint32_t s_cnt[2] = {0, 0}, q_cnt[2] = {0, 0};
+  uint32_t kv_cnt = 0;
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    if (k * (int)gridDim.x >= a.n_items) break;
+    const int x = item_index(k);
+    if (x >= a.n_items) continue;
+    const Item it = decode_item(a, x);
+#pragma unroll
+    for (int slot = 0; slot < 2; ++slot) {
+      if (slot == 1 && !it.valid1) continue;
+      if (!wait_bounded(bar(L::Q_FULL + slot), q_cnt[slot] & 1, abort_flag, a)) { ok = false; break; }
+      ++q_cnt[slot];
+    }
+    if (!ok) break;
+    bool first_pv[2] = {true, true};
+    const int ns = n_steps(a, it);
+    for (int u = 0; u < ns; ++u) {
+      const int kt = step_tile(a, it, u);
+      const bool need[2] = {needs(a, it, 0, kt), needs(a, it, 1, kt)};
+      const int st = kv_cnt % L::NS;
+      const uint32_t ph = (kv_cnt / L::NS) & 1;
+      if (!wait_bounded(bar(L::K_FULL + st), ph, abort_flag, a)) { ok = false; break; }
+      // S_i = Q_i K^T
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        if (!need[slot]) continue;
+        if (s_cnt[slot] > 0 &&
+            !wait_bounded(bar(L::O_FREE + slot), (s_cnt[slot] - 1) & 1, abort_flag, a)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t qa = sbase + L::Q_OFF + slot * L::TILE;
+        const uint32_t kb_ = sbase + L::K_OFF + st * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::BLOCK + (kk & 3) * 32;
+          mma_ss(tmem + L::S_COL(slot), sw128_desc(qa + off, 16, 1024),
+                 sw128_desc(kb_ + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::S_FULL + slot));
+        ++s_cnt[slot];
+      }
+      if (!ok) break;
+      mma_commit(bar(L::K_EMPTY + st));
+      if (u == ns - 1) {
+        mma_commit(bar(L::Q_EMPTY + 0));
+        if (it.valid1) mma_commit(bar(L::Q_EMPTY + 1));
+      }
+      if (!wait_bounded(bar(L::V_FULL + st), ph, abort_flag, a)) { ok = false; break; }
+      // O_i += P_i V
+#pragma unroll
+      for (int slot = 0; slot < 2; ++slot) {
+        if (!need[slot]) continue;
+        if (!wait_bounded(bar(L::P_FULL + slot), (s_cnt[slot] - 1) & 1, abort_flag, a)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vb = sbase + L::V_OFF + st * L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + L::O_COL(slot), tmem + L::S_COL(slot) + kk * 8,
+                 sw128_desc(vb + kk * 2048, L::BLOCK, 1024), idesc_pv,
+                 (first_pv[slot] && kk == 0) ? 0u : 1u);
+        first_pv[slot] = false;
+        mma_commit(bar(L::O_FREE + slot));
+      }
+      if (!ok) break;
+      mma_commit(bar(L::V_EMPTY + st));
+      ++kv_cnt;
+    }
+  }
+  // Every MMA this thread issued completes before tensor memory is freed.
+  mma_commit(bar(L::DONE));
+  wait_drain(bar(L::DONE), 0, a.timeout_ns);
+}
+
+// ------------------------------------------------------ softmax / epilogue
+template <int D>
+__device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
+                             volatile int* abort_flag) {
+  using L = Layout<D>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = warp >> 2;
+  const int r = threadIdx.x & 127;  // row inside the 128-row query tile == TMEM lane
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+  const uint32_t tS = tmem + lane_base + L::S_COL(slot);
+  const uint32_t tO = tmem + lane_base + L::O_COL(slot);
+  const float c = a.scale_log2;
+  const uint64_t c2 = f2_pack(c, c);
+  uint32_t n = 0;  // S tiles consumed so far by this slot
+
+  for (int k = 0;; ++k) {
+    if (k * (int)gridDim.x >= a.n_items) break;
+    const int x = item_index(k);
+    if (x >= a.n_items) continue;
+    const Item it = decode_item(a, x);
+    if (slot == 1 && !it.valid1) continue;
+    const int ns = n_steps(a, it);
+    int u_last = ns - 1;
+    while (u_last > 0 && !needs(a, it, slot, step_tile(a, it, u_last))) --u_last;
+
+    float m = -INFINITY;  // running max (scaled, log2 units) used as the exp2 reference
+    float l = 0.0f;       // running sum of exp2(x - m)
+    bool first = true;
+    for (int u = 0; u < ns; ++u) {
+      const int kt = step_tile(a, it, u);
+      if (!needs(a, it, slot, kt)) continue;
+      if (!wait_warp(bar(L::S_FULL + slot), n & 1, abort_flag, a)) return;
+      tc_fence_after();
+      uint32_t s[128];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tmem_ld32(tS + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * j]));
+      tmem_wait_ld();
+
+      const bool diag = a.causal && kt == it.qt[slot];
+      if (diag) {
+#pragma unroll
+        for (int j = 0; j < 128; ++j)
+          if (j > r) s[j] = __float_as_uint(-INFINITY);
+      }
+      // row max of the raw scores
+      float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
+      float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
+#pragma unroll
+      for (int j = 4; j < 128; j += 8) {
+        mx0 = max3(mx0, __uint_as_float(s[j + 0]), __uint_as_float(s[j + 1]));
+        mx1 = max3(mx1, __uint_as_float(s[j + 2]), __uint_as_float(s[j + 3]));
+        mx2 = max3(mx2, __uint_as_float(s[j + 4]), __uint_as_float(s[j + 5]));
+        mx3 = max3(mx3, __uint_as_float(s[j + 6]), __uint_as_float(s[j + 7]));
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+
+      // online-softmax reference update; O is rescaled only when the max
+      // grows past the threshold (exact either way: l and O share m)
+      float alpha = 1.0f;
+      if (first) {
+        m = mx;
+      } else if (mx > m + kRescaleThreshold) {
+        alpha = ex2(m - mx);
+        m = mx;
+        l *= alpha;
+      }
+      if (!first && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st32(tO + c0, o);
+        }
+      }
+
+      // p = exp2(x*c - m), row sum, pack to bf16 pairs
+      const uint64_t negm2 = f2_pack(-m, -m);
+      uint64_t sum2a = 0, sum2b = 0;
+      uint32_t pk[64];
+#pragma unroll
+      for (int j = 0; j < 128; j += 2) {
+        const uint64_t xs = f2_fma(f2_pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), c2, negm2);
+        float p0 = ex2(f2_lo(xs)), p1 = ex2(f2_hi(xs));
+        if (diag) {
+          if (j > r) p0 = 0.0f;
+          if (j + 1 > r) p1 = 0.0f;
+        }
+        if ((j & 2) == 0) sum2a = f2_add(sum2a, f2_pack(p0, p1));
+        else sum2b = f2_add(sum2b, f2_pack(p0, p1));
+        pk[j >> 1] = pack_bf16x2(p0, p1);
+      }
+      const uint64_t sum2 = f2_add(sum2a, sum2b);
+      l += f2_lo(sum2) + f2_hi(sum2);
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::P_FULL + slot));
+      ++n;
+      first = false;
+
+      if (u == u_last) {
+        // epilogue: wait for the last O_i += P_i V, then out = O / l, lse
+        if (!wait_warp(bar(L::O_FREE + slot), (n - 1) & 1, abort_flag, a)) return;
+        tc_fence_after();
+        const int srow = it.qt[slot] * kBM + r;
+        const int h = it.h[slot];
+        const float inv_l = 1.0f / l;
+        uint4* orow = reinterpret_cast<uint4*>(
+            static_cast<__nv_bfloat16*>(a.out) + (((size_t)it.b * a.S + srow) * a.H + h) * D);
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0, o);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            orow[c0 / 8 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        }
+        if (a.lse)
+          a.lse[((size_t)it.b * a.H + h) * a.S + srow] = (m + log2f(l)) * 0.69314718055994531f;
+        tc_fence_before();
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::N_BARS; ++i) {
+      const bool per_warp = (i == L::P_FULL || i == L::P_FULL + 1);
+      mbar_init(sbase + L::BAR_OFF + 8u * i, per_warp ? 4u : 1u);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == kWarpTma && (threadIdx.x & 31) == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp < 8) {
+    softmax_role<D>(a, sbase, tmem, abort_flag);
+  } else if (warp == kWarpTma) {
+    if ((threadIdx.x & 31) == 0) tma_role<D>(&tm_q, &tm_k, &tm_v, a, sbase, abort_flag);
+  } else {
+    if ((threadIdx.x & 31) == 0) mma_role<D>(a, sbase, tmem, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+size_t fwd_smem_bytes(int D) {
+  return D == 128 ? (size_t)Layout<128>::ALLOC : (size_t)Layout<64>::ALLOC;
+}
+
+template <int D>
+static cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdArgs& args, int grid, cudaStream_t stream) {
+  const int smem = Layout<D>::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(ring_attn_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  ring_attn_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& args, int grid, cudaStream_t stream) {
+  if (D == 128) return launch_d<128>(tq, tk, tv, args, grid, stream);
+  return launch_d<64>(tq, tk, tv, args, grid, stream);
+}
+
+cudaError_t status_word_ptr(unsigned int** p) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_status_word);
+}
+
+cudaError_t read_and_clear_status(unsigned int* value) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_status_word, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_status_word, &zero, sizeof(unsigned int));
+}
+
+}  // namespace ra

@@ -1,0 +1,50 @@
+// ra_internal.h -- declarations shared by the translation units of
+// libringattn (host side only; not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace ra {
+
+// How the two 128-row query tiles a CTA works on at a time are chosen.
+enum PairMode : int {
+  MODE_SINGLE = 0,  // one query tile; the second slot stays idle
+  MODE_HEADS = 1,   // two query heads of the same KV head, same rows
+  MODE_QTILES = 2,  // two consecutive 128-row tiles of one head, same chunk
+};
+
+// Kernel arguments besides the three tensor maps (q, k, v).
+struct FwdArgs {
+  void* out;             // bf16 [B,S,H,D]
+  float* lse;            // fp32 [B,H,S] or nullptr
+  unsigned int* status;  // this device's sticky status word
+  int B, H, Hkv, S, P;
+  int causal;
+  int mode;              // PairMode
+  int tiles;             // S / 128
+  int tpc;               // 128-row tiles per chunk (S / P / 128)
+  int groups;            // work items per query-tile index
+  int nq;                // query-tile indices
+  int n_items;           // groups * nq
+  float scale_log2;      // scale * log2(e)
+  unsigned long long timeout_ns;
+  int skip_value_load;   // failure-path test hook
+};
+
+// status word bits
+constexpr unsigned int kStatusTimeout = 1u;
+
+// ra_fwd.cu
+cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& args, int grid, cudaStream_t stream);
+size_t fwd_smem_bytes(int D);
+cudaError_t status_word_ptr(unsigned int** p);
+cudaError_t read_and_clear_status(unsigned int* value);
+
+// ra_merge.cu
+cudaError_t launch_merge(const void* o_parts, int o_is_fp32, const float* lse_parts, int n,
+                         void* out, float* lse, long long rows, int H, int S, int D, int grid,
+                         cudaStream_t stream);
+
+}  // namespace ra

@@ -18,3 +18,24 @@ def oracle_mod():
 
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def ralib():
+    """The built libringattn (compiled in-tree on first use)."""
+    from ring_chunked_attention_gb300 import build as b
+
+    b.build()
+    import ring_chunked_attention_gb300 as ra
+
+    ra._load()
+    return ra
+
+
+@pytest.fixture(scope="session")
+def cuda_ok():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return True

@@ -1,0 +1,79 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+``include/ringattn.h`` declares, and host-side validation rejects bad
+arguments before touching the device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ringattn.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("ra_fwd", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ralib):
+    lib = ctypes.CDLL(ralib.library_path())
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_status_strings(ralib):
+    assert ralib.ra_status_string(0) == "RA_OK"
+    assert ralib.ra_status_string(4) == "RA_ERR_TIMEOUT"
+    assert ralib.ra_status_string(99) == "RA_ERR_UNKNOWN"
+    assert ralib.ra_version() == (0 << 16) | (1 << 8)
+
+
+# Fake, 16-byte aligned addresses: validation must reject these calls before
+# any CUDA call, so the addresses are never dereferenced.
+Q, K, V, O, L = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+OK_SHAPE = dict(B=1, H=4, Hkv=2, S=256, D=128, P=2, causal=1, scale=0.125)
+
+
+def _call(ralib, q=Q, k=K, v=V, o=O, l=L, **kw):
+    a = dict(OK_SHAPE)
+    a.update(kw)
+    return ralib.ra_fwd_raw(q, k, v, o, l, a["B"], a["H"], a["Hkv"], a["S"], a["D"], a["P"],
+                            a["causal"], a["scale"], stream=0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(k=0), 1), (dict(v=0), 1), (dict(o=0), 1),
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(S=0), 1), (dict(D=0), 1), (dict(P=0), 1),
+    (dict(H=3, Hkv=2), 1),             # H % Hkv != 0
+    (dict(S=256, P=3), 1),             # S % P != 0
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=-0.5), 2),             # negative scale: outside the kernels
+    (dict(D=96), 2), (dict(D=256), 2),
+    (dict(S=384, P=2), 2),             # chunk of 192 rows: not a multiple of 128
+    (dict(S=200, P=1), 2),             # ragged sequence
+    (dict(q=Q + 8), 2), (dict(o=O + 4), 2), (dict(l=L + 2), 2),
+    (dict(B=1 << 16, S=1 << 15, P=1), 2),  # B*S >= 2^31 rows
+])
+def test_fwd_validation_rejects_before_launch(ralib, kw, code):
+    assert _call(ralib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(o=0), 1), (dict(l=0), 1), (dict(out=0), 1), (dict(n=0), 1), (dict(B=0), 1),
+    (dict(D=12), 2), (dict(o=O + 8), 2), (dict(out=O + 8), 2),
+])
+def test_merge_validation_rejects_before_launch(ralib, kw, code):
+    a = dict(o=Q, l=L, n=2, out=O, lse=L + 4096, B=1, H=2, S=128, D=64)
+    a.update(kw)
+    lib = ralib._load()
+    rc = lib.ra_merge_partials(a["o"], 0, a["l"], a["n"], a["out"], a["lse"], a["B"], a["H"],
+                               a["S"], a["D"], None)
+    assert rc == code

@@ -1,0 +1,185 @@
+"""GPU parity of ra_fwd against the fp64 oracle, plus metamorphic checks.
+
+Small cases (oracle on every row) span several 128-row tiles, every work
+pairing the kernel uses (two heads of one GQA group; two consecutive tiles of
+one head; a single tile), causal and non-causal, D = 64 and 128, P = 1 and
+P = S/128 (one tile per chunk).  The five long-context workloads run at full
+size in the launch configuration the benchmark times and are checked on a
+deterministic row sample (chunk boundaries of every head plus seeded random
+rows).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from ring_chunked_attention_gb300.inputs import WORKLOADS, Workload, make_inputs, sample_rows
+from tests.parity import assert_parity, compare
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(ralib, q, k, v, w: Workload, **kw):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    out, lse = ralib.ra_fwd(qd, kd, vd, P=w.P, causal=w.causal, scale=kw.get("scale", w.scale))
+    torch.cuda.synchronize()
+    assert ralib.ra_get_last_device_status() == 0
+    return out, lse
+
+
+SMALL = [
+    # name, B, H, Hkv, S, D, P, causal
+    ("tiny_noncausal_single", 1, 2, 2, 256, 64, 2, False),
+    ("heads_causal_d128", 1, 4, 1, 512, 128, 2, True),
+    ("heads_noncausal_d128", 2, 4, 2, 384, 128, 3, False),
+    ("qtiles_causal_d128", 2, 3, 3, 1024, 128, 4, True),
+    ("qtiles_noncausal_d64", 1, 3, 3, 512, 64, 2, False),
+    ("single_causal_d64_p_eq_tiles", 1, 3, 1, 640, 64, 5, True),
+    ("heads_causal_d64_manychunks", 1, 8, 2, 1024, 64, 8, True),
+    ("qtiles_causal_d128_p1", 1, 1, 1, 768, 128, 1, True),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_parity_all_rows(ralib, cuda_ok, oracle_mod, case):
+    name, B, H, Hkv, S, D, P, causal = case
+    w = Workload(name, B, H, Hkv, S, D, P, causal)
+    q, k, v = make_inputs(w, seed=7)
+    out, lse = _run(ralib, q, k, v, w)
+    o_ref, l_ref = oracle_mod.attn_ring(q, k, v, P, causal, w.scale)
+    st = compare(out, lse, o_ref, l_ref)
+    assert_parity(st, name)
+
+
+def test_tiny_workload_ring_and_direct(ralib, cuda_ok, oracle_mod):
+    w = WORKLOADS["tiny"]
+    q, k, v = make_inputs(w)
+    out, lse = _run(ralib, q, k, v, w)
+    for fn in (oracle_mod.attn_direct, lambda *a: oracle_mod.attn_ring(*a[:3], w.P, *a[3:])):
+        o_ref, l_ref = fn(q, k, v, w.causal, w.scale)
+        assert_parity(compare(out, lse, o_ref, l_ref), "tiny")
+
+
+SAMPLING = {  # every-th row, random rows per (b, h)
+    "causal_s4096": None,  # full oracle
+    "gqa_s16384": (2048, 8),
+    "long_s65536": (8192, 8),
+    "d64_s32768": (4096, 4),
+}
+
+
+@pytest.mark.parametrize("name", list(SAMPLING))
+def test_full_size_workload_parity(ralib, cuda_ok, oracle_mod, name):
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w)
+    out, lse = _run(ralib, q, k, v, w)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    if SAMPLING[name] is None:
+        o_ref, l_ref = oracle_mod.attn_direct(q, k, v, w.causal, w.scale)
+        st = compare(out, lse, o_ref, l_ref)
+    else:
+        every, nr = SAMPLING[name]
+        rows = sample_rows(w, n_random=nr, every=every).numpy()
+        o_ref, l_ref = oracle_mod.attn_direct(q, k, v, w.causal, w.scale, rows=rows)
+        st = compare(out, lse, o_ref, l_ref, rows=rows)
+    print(name, st)
+    assert_parity(st, name)
+
+
+# ---------------------------------------------------------------- metamorphic
+def test_deterministic(ralib, cuda_ok):
+    w = Workload("det", 1, 8, 2, 2048, 128, 4, True)
+    q, k, v = make_inputs(w, seed=3)
+    o1, l1 = _run(ralib, q, k, v, w)
+    o2, l2 = _run(ralib, q, k, v, w)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_future_chunks_do_not_reach_earlier_rows(ralib, cuda_ok, D):
+    w = Workload("fut", 1, 4, 2, 1024, D, 4, True)
+    q, k, v = make_inputs(w, seed=5)
+    o1, l1 = _run(ralib, q, k, v, w)
+    g = torch.Generator().manual_seed(11)
+    C = w.chunk
+    i = 1
+    k2, v2 = k.clone(), v.clone()
+    k2[:, (i + 1) * C:] = torch.randn(k2[:, (i + 1) * C:].shape, generator=g).bfloat16()
+    v2[:, (i + 1) * C:] = torch.randn(v2[:, (i + 1) * C:].shape, generator=g).bfloat16()
+    o2, l2 = _run(ralib, q, k2, v2, w)
+    assert torch.equal(o1[:, : (i + 1) * C], o2[:, : (i + 1) * C])
+    assert torch.equal(l1[:, :, : (i + 1) * C], l2[:, :, : (i + 1) * C])
+    assert not torch.equal(o1[:, (i + 1) * C:], o2[:, (i + 1) * C:])
+
+
+def test_p_invariance(ralib, cuda_ok):
+    base = Workload("pinv", 1, 4, 4, 2048, 128, 1, True)
+    q, k, v = make_inputs(base, seed=9)
+    outs = [_run(ralib, q, k, v, base.with_(P=P)) for P in (1, 2, 4, 16)]
+    o0 = outs[0][0].float()
+    for o, l in outs[1:]:
+        assert (o.float() - o0).abs().max().item() <= 2 * 1.5e-2
+        assert (l - outs[0][1]).abs().max().item() <= 1e-3 * max(1.0, outs[0][1].abs().max().item())
+
+
+def test_gqa_equals_mha_on_repeated_kv(ralib, cuda_ok):
+    w = Workload("gqa", 2, 8, 2, 1024, 128, 4, True)
+    q, k, v = make_inputs(w, seed=13)
+    o1, l1 = _run(ralib, q, k, v, w)
+    rep = w.H // w.Hkv
+    w2 = w.with_(Hkv=w.H)
+    o2, l2 = _run(ralib, q, k.repeat_interleave(rep, 2).contiguous(),
+                  v.repeat_interleave(rep, 2).contiguous(), w2)
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1 - l2).abs().max().item() <= 1e-4 * max(1.0, l1.abs().max().item())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_scale_gives_mean_of_allowed_values(ralib, cuda_ok, oracle_mod, causal):
+    w = Workload("uni", 1, 2, 1, 512, 64, 2, causal)
+    q, k, v = make_inputs(w, seed=17)
+    out, lse = _run(ralib, q, k, v, w, scale=0.0)
+    vd = v.double().numpy()
+    S = w.S
+    if causal:
+        cnt = np.arange(1, S + 1, dtype=np.float64)
+        mean = np.cumsum(vd, axis=1) / cnt[None, :, None, None]
+        lse_ref = np.broadcast_to(np.log(cnt), (1, w.H, S))
+    else:
+        mean = np.broadcast_to(vd.mean(axis=1, keepdims=True), vd.shape)
+        lse_ref = np.full((1, w.H, S), math.log(S))
+    exp_out = np.repeat(mean, w.H // w.Hkv, axis=2)
+    st = compare(out, lse, exp_out, lse_ref)
+    assert_parity(st, "uniform")
+
+
+def test_lse_optional(ralib, cuda_ok):
+    w = Workload("nolse", 1, 2, 2, 256, 128, 2, True)
+    q, k, v = make_inputs(w, seed=19)
+    o1, _ = _run(ralib, q, k, v, w)
+    o2, l2 = ralib.ra_fwd(q.cuda(), k.cuda(), v.cuda(), P=w.P, causal=True, want_lse=False)
+    torch.cuda.synchronize()
+    assert l2 is None and torch.equal(o1, o2)
+
+
+def test_peaked_softmax_rescaling(ralib, cuda_ok, oracle_mod):
+    # std 3 on q and k at D = 128: scores with std 9, max jumps by far more
+    # than the 2^8 rescale threshold inside a row
+    w = Workload("peak", 1, 2, 2, 1024, 128, 4, True, sigma_qk=3.0)
+    q, k, v = make_inputs(w, seed=23)
+    out, lse = _run(ralib, q, k, v, w)
+    o_ref, l_ref = oracle_mod.attn_direct(q, k, v, True, w.scale)
+    assert_parity(compare(out, lse, o_ref, l_ref), "peaked")
+
+
+def test_stream_argument_is_used(ralib, cuda_ok, oracle_mod):
+    w = Workload("stream", 1, 4, 2, 512, 128, 2, True)
+    q, k, v = make_inputs(w, seed=29)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, lse = ralib.ra_fwd(qd, kd, vd, P=w.P, causal=True, stream=s)
+    s.synchronize()
+    o_ref, l_ref = oracle_mod.attn_direct(q, k, v, True, w.scale)
+    assert_parity(compare(out, lse, o_ref, l_ref), "side stream")
