@@ -88,14 +88,15 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (arrival time, csv line)
         self.t = None
+        self.window = (0.0, float("inf"))
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -105,7 +106,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """Restrict the summary to samples that arrived inside [t0, t1]."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -119,7 +124,11 @@ class ClockSampler:
             self.t.join(timeout=2)
         sm, smax, power, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lo, hi = self.window
+        picked = [ln for t, ln in self.lines if lo <= t <= hi + 0.05]
+        if not picked:  # timed region shorter than one sample period
+            picked = [ln for _, ln in self.lines[-3:]]
+        for ln in picked:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -154,7 +163,7 @@ def cpu_oracle_sample(w, budget_s: float = 15.0, seed: int = 0, inputs=None):
 
     q, k, v = inputs if inputs is not None else make_inputs(w)
     threads = oracle.default_threads()
-    rows = sample_rows(w, n_random=256, every=w.S // 4, seed=seed).numpy()
+    rows = sample_rows(w, n_random=1024, every=w.S // 4, seed=seed).numpy()
     rng = np.random.default_rng(seed)
     rows = rng.permutation(rows)
     # calibrate on a small batch, then size the sample to the budget
@@ -259,15 +268,17 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(0.5)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    t_start = time.time()
     for e0, e1 in evs:
         flush.fill_(1.0)
         e0.record(stream)
         step()
         e1.record(stream)
     torch.cuda.synchronize()
+    sampler.mark(t_start, time.time())
     clocks = sampler.stop()
     kernel_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     if ra.ra_get_last_device_status() != 0:
@@ -350,7 +361,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))

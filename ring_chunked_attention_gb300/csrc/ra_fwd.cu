@@ -64,8 +64,8 @@ struct Layout {
   static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
-  static constexpr uint32_t S_COL(int i) { return 128u * i; }
-  static constexpr uint32_t O_COL(int i) { return 256u + (uint32_t)D * i; }
+  __host__ __device__ static constexpr uint32_t S_COL(int i) { return 128u * i; }
+  __host__ __device__ static constexpr uint32_t O_COL(int i) { return 256u + (uint32_t)D * i; }
 };
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
@@ -392,15 +392,18 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           if (j > r) s[j] = __float_as_uint(-INFINITY);
       }
       // row max of the raw scores
+      // four independent 3-input max chains over columns 0..127
       float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
       float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
 #pragma unroll
-      for (int j = 4; j < 128; j += 8) {
+      for (int j = 4; j < 124; j += 8) {
         mx0 = max3(mx0, __uint_as_float(s[j + 0]), __uint_as_float(s[j + 1]));
         mx1 = max3(mx1, __uint_as_float(s[j + 2]), __uint_as_float(s[j + 3]));
         mx2 = max3(mx2, __uint_as_float(s[j + 4]), __uint_as_float(s[j + 5]));
         mx3 = max3(mx3, __uint_as_float(s[j + 6]), __uint_as_float(s[j + 7]));
       }
+      mx0 = max3(mx0, __uint_as_float(s[124]), __uint_as_float(s[125]));
+      mx1 = max3(mx1, __uint_as_float(s[126]), __uint_as_float(s[127]));
       const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
 
       // online-softmax reference update; O is rescaled only when the max
@@ -425,7 +428,9 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         }
       }
 
-      // p = exp2(x*c - m), row sum, pack to bf16 pairs
+      // p = exp2(x*c - m), rounded to bf16 pairs for the PV MMA.  The row
+      // sum adds the same rounded values, so that O and l are normalised
+      // consistently (a row dominated by one key returns that value row).
       const uint64_t negm2 = f2_pack(-m, -m);
       uint64_t sum2a = 0, sum2b = 0;
       uint32_t pk[64];
@@ -437,9 +442,11 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           if (j > r) p0 = 0.0f;
           if (j + 1 > r) p1 = 0.0f;
         }
-        if ((j & 2) == 0) sum2a = f2_add(sum2a, f2_pack(p0, p1));
-        else sum2b = f2_add(sum2b, f2_pack(p0, p1));
-        pk[j >> 1] = pack_bf16x2(p0, p1);
+        const uint32_t pr = pack_bf16x2(p0, p1);
+        const uint64_t pr2 = ((uint64_t)(pr & 0xFFFF0000u) << 32) | (uint64_t)(pr << 16);
+        if ((j & 2) == 0) sum2a = f2_add(sum2a, pr2);
+        else sum2b = f2_add(sum2b, pr2);
+        pk[j >> 1] = pr;
       }
       const uint64_t sum2 = f2_add(sum2a, sum2b);
       l += f2_lo(sum2) + f2_hi(sum2);

@@ -1,7 +1,16 @@
-"""Comparison helpers for GPU-vs-oracle parity (tolerances of the method's
-accuracy target: bf16 O within 1.5e-2 max-abs and 2e-3 mean-abs of the fp64
-oracle for V ~ N(0,1); LSE within 1e-3 relative, read as
-|d lse| <= 1e-3 * max(1, |lse|) so that rows with lse near 0 stay meaningful)."""
+"""Comparison helpers for GPU-vs-oracle parity.
+
+Tolerances (the method's accuracy target): bf16 O within 1.5e-2 max-abs and
+2e-3 mean-abs of the fp64 oracle for V ~ N(0,1); LSE within 1e-3 relative,
+read as |d lse| <= 1e-3 * max(1, |lse|) so that rows with lse near 0 stay
+meaningful.
+
+Attribution of the one exception: O is returned in bf16, whose half-ulp is
+2^-6 = 0.0156 > 1.5e-2 for |O| in [4, 8).  An element whose GPU value is
+exactly bf16_rne(oracle) -- the best bf16 answer there is -- can therefore
+sit past 1.5e-2 through output rounding alone.  Such elements are counted and
+reported (``n_rounding_only``); every other element must meet the gate.
+"""
 import numpy as np
 import torch
 
@@ -33,10 +42,14 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None):
     err = np.abs(o - out_ref)
     st = {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
           "finite": bool(np.isfinite(o).all())}
-    # error of the ideal bf16 rounding of the oracle, for attribution
+    # the ideal bf16 rounding of the oracle, for attribution
     ref_bf16 = torch.tensor(out_ref).to(torch.bfloat16).double().numpy()
     st["max_abs_vs_rounded_ref"] = float(np.abs(o - ref_bf16).max())
-    st["n_ref_ge4_at_max"] = int(((err > MAX_ABS) & (np.abs(out_ref) >= 4)).sum())
+    over = err > MAX_ABS
+    rounding_only = over & (o == ref_bf16)
+    st["n_over_gate"] = int(over.sum())
+    st["n_rounding_only"] = int(rounding_only.sum())
+    st["max_abs_unattributed"] = float(np.where(rounding_only, 0.0, err).max())
     if l is not None:
         dl = np.abs(l - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
         st["lse_rel"] = float(dl.max())
@@ -45,7 +58,9 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None):
 
 def assert_parity(st, what=""):
     assert st["finite"], f"{what}: non-finite output"
-    assert st["max_abs"] <= MAX_ABS, f"{what}: max-abs {st['max_abs']:.3e} > {MAX_ABS} ({st})"
+    assert st["max_abs_unattributed"] <= MAX_ABS, (
+        f"{what}: max-abs {st['max_abs_unattributed']:.3e} > {MAX_ABS} on elements that are not the "
+        f"correctly rounded bf16 value ({st})")
     assert st["mean_abs"] <= MEAN_ABS, f"{what}: mean-abs {st['mean_abs']:.3e} > {MEAN_ABS} ({st})"
     if "lse_rel" in st:
         assert st["lse_rel"] <= LSE_REL, f"{what}: lse rel {st['lse_rel']:.3e} > {LSE_REL} ({st})"
