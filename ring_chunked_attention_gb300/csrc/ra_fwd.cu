@@ -260,86 +260,146 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 }
 
 // ---------------------------------------------------------------- MMA issuer
+// Issue order per key/value step u, for each query slot in turn:
+//   O_i += P_i(u) V(u)          once the softmax has written P_i(u)
+//   S_i(u+1) = Q_i K(u+1)^T     once that PV has completed (P_i aliases S_i)
+// so each slot's chain (softmax -> PV -> next S) runs independently of the
+// other slot's softmax, and the tensor pipe alternates between the two.
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int slot, int st) {
+  using L = Layout<D>;
+  constexpr uint32_t idesc_s = make_idesc(kBM, kBN, 0);
+  const uint32_t qa = sbase + L::Q_OFF + slot * L::TILE;
+  const uint32_t ka = sbase + L::K_OFF + st * L::TILE;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * L::BLOCK + (kk & 3) * 32;
+    mma_ss(tmem + L::S_COL(slot), sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024),
+           idesc_s, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int slot, int st,
+                                         bool accumulate) {
+  using L = Layout<D>;
+  constexpr uint32_t idesc_pv = make_idesc(kBM, D, 1);
+  const uint32_t va = sbase + L::V_OFF + st * L::TILE;
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk)
+    mma_ts(tmem + L::O_COL(slot), tmem + L::S_COL(slot) + kk * 8,
+           sw128_desc(va + kk * 2048, L::BLOCK, 1024), idesc_pv,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
+
 template <int D>
 __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
                          volatile int* abort_flag) {
   using L = Layout<D>;
   auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
-  constexpr uint32_t idesc_s = make_idesc(kBM, kBN, 0);
-  constexpr uint32_t idesc_pv = make_idesc(kBM, D, 1);
-  uint32_t s_cnt[2] = {0, 0}, q_cnt[2] = {0, 0};
-  uint32_t kv_cnt = 0;
+  uint32_t s_cnt0 = 0, s_cnt1 = 0;  // S MMAs issued per slot (== PV MMAs once a step is done)
+  uint32_t q_cnt0 = 0, q_cnt1 = 0;
+  uint32_t kv_cnt = 0;              // K/V ring position of step 0 of the current item
   bool ok = true;
+
+  // S_i(u) for every slot that needs step u; waits for its previous PV first.
+  auto s_step = [&](const Item& it, int u) -> bool {
+    const int kt = step_tile(a, it, u);
+    const uint32_t c = kv_cnt + u;
+    const int st = c % L::NS;
+    if (!wait_bounded(bar(L::K_FULL + st), (c / L::NS) & 1, abort_flag, a)) return false;
+    if (needs(a, it, 0, kt)) {
+      if (s_cnt0 > 0 && !wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a))
+        return false;
+      tc_fence_after();
+      issue_s<D>(tmem, sbase, 0, st);
+      mma_commit(bar(L::S_FULL + 0));
+      ++s_cnt0;
+    }
+    if (needs(a, it, 1, kt)) {
+      if (s_cnt1 > 0 && !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a))
+        return false;
+      tc_fence_after();
+      issue_s<D>(tmem, sbase, 1, st);
+      mma_commit(bar(L::S_FULL + 1));
+      ++s_cnt1;
+    }
+    mma_commit(bar(L::K_EMPTY + st));
+    return true;
+  };
+
   for (int k = 0; ok; ++k) {
     if (k * (int)gridDim.x >= a.n_items) break;
     const int x = item_index(k);
     if (x >= a.n_items) continue;
     const Item it = decode_item(a, x);
-#pragma unroll
-    for (int slot = 0; slot < 2; ++slot) {
-      if (slot == 1 && !it.valid1) continue;
-      if (!wait_bounded(bar(L::Q_FULL + slot), q_cnt[slot] & 1, abort_flag, a)) { ok = false; break; }
-      ++q_cnt[slot];
+    if (!wait_bounded(bar(L::Q_FULL + 0), q_cnt0 & 1, abort_flag, a)) break;
+    ++q_cnt0;
+    if (it.valid1) {
+      if (!wait_bounded(bar(L::Q_FULL + 1), q_cnt1 & 1, abort_flag, a)) break;
+      ++q_cnt1;
     }
-    if (!ok) break;
-    bool first_pv[2] = {true, true};
     const int ns = n_steps(a, it);
-    for (int u = 0; u < ns; ++u) {
+    if (!s_step(it, 0)) break;
+    if (ns == 1) {
+      mma_commit(bar(L::Q_EMPTY + 0));
+      if (it.valid1) mma_commit(bar(L::Q_EMPTY + 1));
+    }
+    bool first0 = true, first1 = true;
+    for (int u = 0; u < ns && ok; ++u) {
       const int kt = step_tile(a, it, u);
-      const bool need[2] = {needs(a, it, 0, kt), needs(a, it, 1, kt)};
-      const int st = kv_cnt % L::NS;
-      const uint32_t ph = (kv_cnt / L::NS) & 1;
-      if (!wait_bounded(bar(L::K_FULL + st), ph, abort_flag, a)) { ok = false; break; }
-      // S_i = Q_i K^T
-#pragma unroll
-      for (int slot = 0; slot < 2; ++slot) {
-        if (!need[slot]) continue;
-        if (s_cnt[slot] > 0 &&
-            !wait_bounded(bar(L::O_FREE + slot), (s_cnt[slot] - 1) & 1, abort_flag, a)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t qa = sbase + L::Q_OFF + slot * L::TILE;
-        const uint32_t kb_ = sbase + L::K_OFF + st * L::TILE;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::BLOCK + (kk & 3) * 32;
-          mma_ss(tmem + L::S_COL(slot), sw128_desc(qa + off, 16, 1024),
-                 sw128_desc(kb_ + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::S_FULL + slot));
-        ++s_cnt[slot];
+      const uint32_t c = kv_cnt + u;
+      const int st = c % L::NS;
+      const bool n0 = needs(a, it, 0, kt), n1 = needs(a, it, 1, kt);
+      const bool more = u + 1 < ns;
+      const int kt1 = more ? step_tile(a, it, u + 1) : 0;
+      const bool m0 = more && needs(a, it, 0, kt1), m1 = more && needs(a, it, 1, kt1);
+      if (!wait_bounded(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+      int st1 = -1;
+      if (more) {
+        const uint32_t c1 = c + 1;
+        st1 = c1 % L::NS;
+        if (!wait_bounded(bar(L::K_FULL + st1), (c1 / L::NS) & 1, abort_flag, a)) { ok = false; break; }
       }
-      if (!ok) break;
-      mma_commit(bar(L::K_EMPTY + st));
-      if (u == ns - 1) {
+      // slot 0: PV(u), then S(u+1)
+      if (n0) {
+        if (!wait_bounded(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv<D>(tmem, sbase, 0, st, !first0);
+        mma_commit(bar(L::O_FREE + 0));
+        first0 = false;
+      }
+      if (m0) {
+        if (!wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+        tc_fence_after();
+        issue_s<D>(tmem, sbase, 0, st1);
+        mma_commit(bar(L::S_FULL + 0));
+        ++s_cnt0;
+      }
+      // slot 1: PV(u), then S(u+1)
+      if (n1) {
+        if (!wait_bounded(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv<D>(tmem, sbase, 1, st, !first1);
+        mma_commit(bar(L::O_FREE + 1));
+        first1 = false;
+      }
+      if (m1) {
+        if (s_cnt1 > 0 &&
+            !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+        tc_fence_after();
+        issue_s<D>(tmem, sbase, 1, st1);
+        mma_commit(bar(L::S_FULL + 1));
+        ++s_cnt1;
+      }
+      mma_commit(bar(L::V_EMPTY + st));
+      if (more) mma_commit(bar(L::K_EMPTY + st1));
+      if (u + 2 == ns) {  // the item's last S MMAs are issued: its Q tiles may be replaced
         mma_commit(bar(L::Q_EMPTY + 0));
         if (it.valid1) mma_commit(bar(L::Q_EMPTY + 1));
       }
-      if (!wait_bounded(bar(L::V_FULL + st), ph, abort_flag, a)) { ok = false; break; }
-      // O_i += P_i V
-#pragma unroll
-      for (int slot = 0; slot < 2; ++slot) {
-        if (!need[slot]) continue;
-        if (!wait_bounded(bar(L::P_FULL + slot), (s_cnt[slot] - 1) & 1, abort_flag, a)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t vb = sbase + L::V_OFF + st * L::TILE;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + L::O_COL(slot), tmem + L::S_COL(slot) + kk * 8,
-                 sw128_desc(vb + kk * 2048, L::BLOCK, 1024), idesc_pv,
-                 (first_pv[slot] && kk == 0) ? 0u : 1u);
-        first_pv[slot] = false;
-        mma_commit(bar(L::O_FREE + slot));
-      }
-      if (!ok) break;
-      mma_commit(bar(L::V_EMPTY + st));
-      ++kv_cnt;
     }
+    kv_cnt += ns;
   }
   // Every MMA this thread issued completes before tensor memory is freed.
   mma_commit(bar(L::DONE));
@@ -347,6 +407,131 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
 }
 
 // ------------------------------------------------------ softmax / epilogue
+// Row max of one 32-column chunk of raw scores (columns j0..j0+31); on the
+// diagonal tile, columns past the row are masked out.
+template <bool DIAG>
+__device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], int j0, int r, float mx) {
+  float a0 = mx, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; j += 8) {
+    float x[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      x[t] = __uint_as_float(v[j + t]);
+      if (DIAG && j0 + j + t > r) x[t] = -INFINITY;
+    }
+    a0 = max3(a0, x[0], x[1]);
+    a1 = max3(a1, x[2], x[3]);
+    a2 = max3(a2, x[4], x[5]);
+    a3 = max3(a3, x[6], x[7]);
+  }
+  return fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+}
+
+// p = exp2(x*c - m) for one 32-column chunk; packs bf16 pairs into pk and
+// accumulates both the exact fp32 sum (for lse) and the sum of the rounded
+// values that the PV product consumes (for the output normalisation).
+template <bool DIAG>
+__device__ __forceinline__ void chunk_exp(const uint32_t (&v)[32], int j0, int r, uint64_t c2,
+                                          uint64_t negm2, uint64_t& se0, uint64_t& se1,
+                                          uint64_t& sr0, uint64_t& sr1, uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const uint64_t xs = f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), c2, negm2);
+    float p0 = ex2(f2_lo(xs)), p1 = ex2(f2_hi(xs));
+    if (DIAG) {
+      p0 = (j0 + j > r) ? 0.0f : p0;
+      p1 = (j0 + j + 1 > r) ? 0.0f : p1;
+    }
+    const uint32_t pr = pack_bf16x2(p0, p1);
+    const uint64_t prf = ((uint64_t)(pr & 0xFFFF0000u) << 32) | (uint64_t)(pr << 16);
+    if ((j & 2) == 0) {
+      se0 = f2_add(se0, f2_pack(p0, p1));
+      sr0 = f2_add(sr0, prf);
+    } else {
+      se1 = f2_add(se1, f2_pack(p0, p1));
+      sr1 = f2_add(sr1, prf);
+    }
+    pk[j >> 1] = pr;
+  }
+}
+
+struct RowState {
+  float m;        // reference max (scaled, log2 units)
+  float l_exact;  // sum of exp2(x - m) in fp32
+  float l_round;  // sum of the bf16-rounded exp2(x - m)
+};
+
+// One S tile of one slot: max, optional O rescale, exp, P -> TMEM.
+template <int D, bool DIAG>
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, float c, bool first,
+                                             RowState& st) {
+  uint32_t va[32], vb[32];
+  // pass 1: row max, one chunk in flight while the previous one is reduced
+  tmem_ld32(tS + 0, va);
+  tmem_wait_ld_regs(va);
+  tmem_ld32(tS + 32, vb);
+  float mx = chunk_max<DIAG>(va, 0, r, -INFINITY);
+  tmem_wait_ld_regs(vb);
+  tmem_ld32(tS + 64, va);
+  mx = chunk_max<DIAG>(vb, 32, r, mx);
+  tmem_wait_ld_regs(va);
+  tmem_ld32(tS + 96, vb);
+  mx = chunk_max<DIAG>(va, 64, r, mx);
+  tmem_wait_ld_regs(vb);
+  mx = chunk_max<DIAG>(vb, 96, r, mx);
+  tmem_ld32(tS + 0, va);  // pass 2 starts; overlaps the max bookkeeping below
+  mx *= c;
+
+  // reference-max update; O is rescaled only when the max grows past the
+  // threshold (exact either way: l and O always share the same m)
+  float alpha = 1.0f;
+  if (first) {
+    st.m = mx;
+  } else if (mx > st.m + kRescaleThreshold) {
+    alpha = ex2(st.m - mx);
+    st.m = mx;
+    st.l_exact *= alpha;
+    st.l_round *= alpha;
+  }
+  tmem_wait_ld_regs(va);
+  if (!first && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t o[32];
+      tmem_ld32(tO + c0, o);
+      tmem_wait_ld_regs(o);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+      tmem_st32(tO + c0, o);
+    }
+  }
+
+  // pass 2: exp2, sums, bf16 P written over the consumed S columns
+  const uint64_t c2 = f2_pack(c, c);
+  const uint64_t negm2 = f2_pack(-st.m, -st.m);
+  uint64_t se0 = 0, se1 = 0, sr0 = 0, sr1 = 0;
+  uint32_t pk[16];
+  tmem_ld32(tS + 32, vb);
+  chunk_exp<DIAG>(va, 0, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  tmem_st16(tS + 0, pk);
+  tmem_wait_ld_regs(vb);
+  tmem_ld32(tS + 64, va);
+  chunk_exp<DIAG>(vb, 32, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  tmem_st16(tS + 16, pk);
+  tmem_wait_ld_regs(va);
+  tmem_ld32(tS + 96, vb);
+  chunk_exp<DIAG>(va, 64, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  tmem_st16(tS + 32, pk);
+  tmem_wait_ld_regs(vb);
+  chunk_exp<DIAG>(vb, 96, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  tmem_st16(tS + 48, pk);
+  const uint64_t se = f2_add(se0, se1), sr = f2_add(sr0, sr1);
+  st.l_exact += f2_lo(se) + f2_hi(se);
+  st.l_round += f2_lo(sr) + f2_hi(sr);
+  tmem_wait_st();
+}
+
 template <int D>
 __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
                              volatile int* abort_flag) {
@@ -359,7 +544,6 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   const uint32_t tS = tmem + lane_base + L::S_COL(slot);
   const uint32_t tO = tmem + lane_base + L::O_COL(slot);
   const float c = a.scale_log2;
-  const uint64_t c2 = f2_pack(c, c);
   uint32_t n = 0;  // S tiles consumed so far by this slot
 
   for (int k = 0;; ++k) {
@@ -372,87 +556,17 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     int u_last = ns - 1;
     while (u_last > 0 && !needs(a, it, slot, step_tile(a, it, u_last))) --u_last;
 
-    float m = -INFINITY;  // running max (scaled, log2 units) used as the exp2 reference
-    float l = 0.0f;       // running sum of exp2(x - m)
+    RowState st{-INFINITY, 0.0f, 0.0f};
     bool first = true;
     for (int u = 0; u < ns; ++u) {
       const int kt = step_tile(a, it, u);
       if (!needs(a, it, slot, kt)) continue;
       if (!wait_warp(bar(L::S_FULL + slot), n & 1, abort_flag, a)) return;
       tc_fence_after();
-      uint32_t s[128];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tmem_ld32(tS + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * j]));
-      tmem_wait_ld();
-
-      const bool diag = a.causal && kt == it.qt[slot];
-      if (diag) {
-#pragma unroll
-        for (int j = 0; j < 128; ++j)
-          if (j > r) s[j] = __float_as_uint(-INFINITY);
-      }
-      // row max of the raw scores
-      // four independent 3-input max chains over columns 0..127
-      float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
-      float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
-#pragma unroll
-      for (int j = 4; j < 124; j += 8) {
-        mx0 = max3(mx0, __uint_as_float(s[j + 0]), __uint_as_float(s[j + 1]));
-        mx1 = max3(mx1, __uint_as_float(s[j + 2]), __uint_as_float(s[j + 3]));
-        mx2 = max3(mx2, __uint_as_float(s[j + 4]), __uint_as_float(s[j + 5]));
-        mx3 = max3(mx3, __uint_as_float(s[j + 6]), __uint_as_float(s[j + 7]));
-      }
-      mx0 = max3(mx0, __uint_as_float(s[124]), __uint_as_float(s[125]));
-      mx1 = max3(mx1, __uint_as_float(s[126]), __uint_as_float(s[127]));
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
-
-      // online-softmax reference update; O is rescaled only when the max
-      // grows past the threshold (exact either way: l and O share m)
-      float alpha = 1.0f;
-      if (first) {
-        m = mx;
-      } else if (mx > m + kRescaleThreshold) {
-        alpha = ex2(m - mx);
-        m = mx;
-        l *= alpha;
-      }
-      if (!first && __any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + c0, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tmem_st32(tO + c0, o);
-        }
-      }
-
-      // p = exp2(x*c - m), rounded to bf16 pairs for the PV MMA.  The row
-      // sum adds the same rounded values, so that O and l are normalised
-      // consistently (a row dominated by one key returns that value row).
-      const uint64_t negm2 = f2_pack(-m, -m);
-      uint64_t sum2a = 0, sum2b = 0;
-      uint32_t pk[64];
-#pragma unroll
-      for (int j = 0; j < 128; j += 2) {
-        const uint64_t xs = f2_fma(f2_pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), c2, negm2);
-        float p0 = ex2(f2_lo(xs)), p1 = ex2(f2_hi(xs));
-        if (diag) {
-          if (j > r) p0 = 0.0f;
-          if (j + 1 > r) p1 = 0.0f;
-        }
-        const uint32_t pr = pack_bf16x2(p0, p1);
-        const uint64_t pr2 = ((uint64_t)(pr & 0xFFFF0000u) << 32) | (uint64_t)(pr << 16);
-        if ((j & 2) == 0) sum2a = f2_add(sum2a, pr2);
-        else sum2b = f2_add(sum2b, pr2);
-        pk[j >> 1] = pr;
-      }
-      const uint64_t sum2 = f2_add(sum2a, sum2b);
-      l += f2_lo(sum2) + f2_hi(sum2);
-      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      tmem_wait_st();
+      if (a.causal && kt == it.qt[slot])
+        softmax_tile<D, true>(tS, tO, r, c, first, st);
+      else
+        softmax_tile<D, false>(tS, tO, r, c, first, st);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::P_FULL + slot));
@@ -465,14 +579,14 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         tc_fence_after();
         const int srow = it.qt[slot] * kBM + r;
         const int h = it.h[slot];
-        const float inv_l = 1.0f / l;
+        const float inv_l = 1.0f / st.l_round;
         uint4* orow = reinterpret_cast<uint4*>(
             static_cast<__nv_bfloat16*>(a.out) + (((size_t)it.b * a.S + srow) * a.H + h) * D);
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
           tmem_ld32(tO + c0, o);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(o);
           uint32_t w[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
@@ -482,7 +596,8 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
             orow[c0 / 8 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
         if (a.lse)
-          a.lse[((size_t)it.b * a.H + h) * a.S + srow] = (m + log2f(l)) * 0.69314718055994531f;
+          a.lse[((size_t)it.b * a.H + h) * a.S + srow] =
+              (st.m + log2f(st.l_exact)) * 0.69314718055994531f;
         tc_fence_before();
       }
     }
