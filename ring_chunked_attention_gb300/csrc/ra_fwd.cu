@@ -75,12 +75,6 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, int b_mn_major) 
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
 struct Item {
   int b, kvh;
   int h[2];
@@ -134,22 +128,39 @@ __device__ __forceinline__ int n_steps(const FwdArgs& a, const Item& it) {
   return a.causal ? qmax_of(it) + 1 : a.tiles;
 }
 
-// Key tile visited at step u: chunks in ring order starting from the query
-// tiles' own chunk i (i, i-1, i-2, ... wrapping for non-causal); inside a
-// chunk the tiles ascend; causal stops the own chunk at the diagonal tile and
-// never visits chunks after i.
-__device__ __forceinline__ int step_tile(const FwdArgs& a, const Item& it, int u) {
-  const int ci = it.qt[0] / a.tpc;
-  if (a.causal) {
-    const int nd = qmax_of(it) - ci * a.tpc + 1;
-    if (u < nd) return ci * a.tpc + u;
-    u -= nd;
-    const int j = ci - 1 - u / a.tpc;
-    return j * a.tpc + u % a.tpc;
+// Walks the key tiles of one work item in ring order: chunks from the query
+// tiles' own chunk i downwards (i, i-1, i-2, ..., wrapping for non-causal),
+// tiles ascending inside a chunk; causal stops the own chunk at the diagonal
+// tile and never visits chunks after i.  One division per item, none per step.
+struct StepCursor {
+  int kt;    // current key tile
+  int left;  // tiles left in the current chunk, kt included
+  int j;     // current chunk
+  int tpc, P;
+  __device__ __forceinline__ void init(const FwdArgs& a, const Item& it) {
+    tpc = a.tpc;
+    P = a.P;
+    j = it.qt[0] / a.tpc;
+    kt = j * tpc;
+    left = a.causal ? qmax_of(it) - kt + 1 : tpc;
   }
-  int j = ci - u / a.tpc;
-  if (j < 0) j += a.P;
-  return j * a.tpc + u % a.tpc;
+  __device__ __forceinline__ void next() {
+    if (--left > 0) {
+      ++kt;
+      return;
+    }
+    j = (j == 0) ? P - 1 : j - 1;
+    kt = j * tpc;
+    left = tpc;
+  }
+};
+
+// Key tile of the item's last step.
+__device__ __forceinline__ int last_tile(const FwdArgs& a, const Item& it) {
+  const int ci = it.qt[0] / a.tpc;
+  if (a.causal) return ci > 0 ? a.tpc - 1 : qmax_of(it);
+  const int j = (ci + 1 == a.P) ? 0 : ci + 1;
+  return j * a.tpc + a.tpc - 1;
 }
 
 __device__ __forceinline__ bool needs(const FwdArgs& a, const Item& it, int slot, int kt) {
@@ -162,8 +173,8 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
                                        unsigned long long timeout_ns, unsigned int* status) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    if ((it & 3u) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > timeout_ns) {
         if (status) atomicOr(status, kStatusTimeout);
@@ -228,8 +239,10 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
       ++q_cnt[slot];
     }
     const int ns = n_steps(a, it);
-    for (int u = 0; u < ns && ok; ++u) {
-      const int kt = step_tile(a, it, u);
+    StepCursor cur;
+    cur.init(a, it);
+    for (int u = 0; u < ns && ok; ++u, cur.next()) {
+      const int kt = cur.kt;
       const int st = kv_cnt % L::NS;
       const uint32_t ph = (kv_cnt / L::NS) & 1;
       const int row = it.b * a.S + kt * kBN;
@@ -265,31 +278,35 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 //   S_i(u+1) = Q_i K(u+1)^T     once that PV has completed (P_i aliases S_i)
 // so each slot's chain (softmax -> PV -> next S) runs independently of the
 // other slot's softmax, and the tensor pipe alternates between the two.
+// A tcgen05.mma issue blocks for about the MMA's own execution time, so the
+// issuing thread keeps the work between consecutive MMAs to a few integer
+// operations: descriptors are precomputed halves plus immediate offsets, and
+// the step sequence comes from a division-free cursor.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+// high word of a 128-byte-swizzle descriptor: stride byte offset 1024 B
+// (8 rows of 128 B), descriptor version 1, swizzle mode 128 B
+constexpr uint32_t kDescHiSw128 = ((1024u >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int slot, int st) {
+__device__ __forceinline__ void issue_s(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {
   using L = Layout<D>;
   constexpr uint32_t idesc_s = make_idesc(kBM, kBN, 0);
-  const uint32_t qa = sbase + L::Q_OFF + slot * L::TILE;
-  const uint32_t ka = sbase + L::K_OFF + st * L::TILE;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * L::BLOCK + (kk & 3) * 32;
-    mma_ss(tmem + L::S_COL(slot), sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024),
-           idesc_s, kk > 0 ? 1u : 0u);
+    const uint32_t off = (uint32_t)((kk >> 2) * L::BLOCK + (kk & 3) * 32) >> 4;
+    mma_ss_lh(tS, q_lo + off, kDescHiSw128, k_lo + off, kDescHiSw128, idesc_s, kk > 0 ? 1u : 0u);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int slot, int st,
-                                         bool accumulate) {
-  using L = Layout<D>;
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo, bool accumulate) {
   constexpr uint32_t idesc_pv = make_idesc(kBM, D, 1);
-  const uint32_t va = sbase + L::V_OFF + st * L::TILE;
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk)
-    mma_ts(tmem + L::O_COL(slot), tmem + L::S_COL(slot) + kk * 8,
-           sw128_desc(va + kk * 2048, L::BLOCK, 1024), idesc_pv,
-           (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts_lh(tO, tP + kk * 8, v_lo + (uint32_t)(kk * (2048 >> 4)), kDescHiSw128, idesc_pv,
+              (accumulate || kk > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -297,36 +314,17 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
                          volatile int* abort_flag) {
   using L = Layout<D>;
   auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const uint32_t tS0 = tmem + L::S_COL(0), tS1 = tmem + L::S_COL(1);
+  const uint32_t tO0 = tmem + L::O_COL(0), tO1 = tmem + L::O_COL(1);
+  const uint32_t q_lo0 = desc_lo(sbase + L::Q_OFF, 16);
+  const uint32_t q_lo1 = desc_lo(sbase + L::Q_OFF + L::TILE, 16);
+  const uint32_t k_lo0 = desc_lo(sbase + L::K_OFF, 16);
+  const uint32_t v_lo0 = desc_lo(sbase + L::V_OFF, L::BLOCK);
+  constexpr uint32_t kStageLo = (uint32_t)L::TILE >> 4;  // descriptor step between ring stages
   uint32_t s_cnt0 = 0, s_cnt1 = 0;  // S MMAs issued per slot (== PV MMAs once a step is done)
   uint32_t q_cnt0 = 0, q_cnt1 = 0;
-  uint32_t kv_cnt = 0;              // K/V ring position of step 0 of the current item
+  uint32_t c = 0;                   // ring position of the current step
   bool ok = true;
-
-  // S_i(u) for every slot that needs step u; waits for its previous PV first.
-  auto s_step = [&](const Item& it, int u) -> bool {
-    const int kt = step_tile(a, it, u);
-    const uint32_t c = kv_cnt + u;
-    const int st = c % L::NS;
-    if (!wait_bounded(bar(L::K_FULL + st), (c / L::NS) & 1, abort_flag, a)) return false;
-    if (needs(a, it, 0, kt)) {
-      if (s_cnt0 > 0 && !wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a))
-        return false;
-      tc_fence_after();
-      issue_s<D>(tmem, sbase, 0, st);
-      mma_commit(bar(L::S_FULL + 0));
-      ++s_cnt0;
-    }
-    if (needs(a, it, 1, kt)) {
-      if (s_cnt1 > 0 && !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a))
-        return false;
-      tc_fence_after();
-      issue_s<D>(tmem, sbase, 1, st);
-      mma_commit(bar(L::S_FULL + 1));
-      ++s_cnt1;
-    }
-    mma_commit(bar(L::K_EMPTY + st));
-    return true;
-  };
 
   for (int k = 0; ok; ++k) {
     if (k * (int)gridDim.x >= a.n_items) break;
@@ -340,39 +338,55 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       ++q_cnt1;
     }
     const int ns = n_steps(a, it);
-    if (!s_step(it, 0)) break;
-    if (ns == 1) {
-      mma_commit(bar(L::Q_EMPTY + 0));
-      if (it.valid1) mma_commit(bar(L::Q_EMPTY + 1));
+    StepCursor nxt;  // the step whose S MMAs are issued next
+    nxt.init(a, it);
+    // prologue: S(0) for both slots
+    {
+      const int st = c % L::NS;
+      if (!wait_bounded(bar(L::K_FULL + st), (c / L::NS) & 1, abort_flag, a)) break;
+      if (needs(a, it, 0, nxt.kt)) {
+        if (s_cnt0 > 0 && !wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) break;
+        tc_fence_after();
+        issue_s<D>(tS0, q_lo0, k_lo0 + st * kStageLo);
+        mma_commit(bar(L::S_FULL + 0));
+        ++s_cnt0;
+      }
+      if (needs(a, it, 1, nxt.kt)) {
+        if (s_cnt1 > 0 && !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) break;
+        tc_fence_after();
+        issue_s<D>(tS1, q_lo1, k_lo0 + st * kStageLo);
+        mma_commit(bar(L::S_FULL + 1));
+        ++s_cnt1;
+      }
+      mma_commit(bar(L::K_EMPTY + st));
+      if (ns == 1) {
+        mma_commit(bar(L::Q_EMPTY + 0));
+        if (it.valid1) mma_commit(bar(L::Q_EMPTY + 1));
+      }
     }
     bool first0 = true, first1 = true;
-    for (int u = 0; u < ns && ok; ++u) {
-      const int kt = step_tile(a, it, u);
-      const uint32_t c = kv_cnt + u;
+    for (int u = 0; u < ns && ok; ++u, ++c) {
       const int st = c % L::NS;
-      const bool n0 = needs(a, it, 0, kt), n1 = needs(a, it, 1, kt);
+      const bool n0 = needs(a, it, 0, nxt.kt), n1 = needs(a, it, 1, nxt.kt);
       const bool more = u + 1 < ns;
-      const int kt1 = more ? step_tile(a, it, u + 1) : 0;
-      const bool m0 = more && needs(a, it, 0, kt1), m1 = more && needs(a, it, 1, kt1);
+      if (more) nxt.next();
+      const bool m0 = more && needs(a, it, 0, nxt.kt), m1 = more && needs(a, it, 1, nxt.kt);
+      const int st1 = (c + 1) % L::NS;
       if (!wait_bounded(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
-      int st1 = -1;
-      if (more) {
-        const uint32_t c1 = c + 1;
-        st1 = c1 % L::NS;
-        if (!wait_bounded(bar(L::K_FULL + st1), (c1 / L::NS) & 1, abort_flag, a)) { ok = false; break; }
-      }
+      if (more &&
+          !wait_bounded(bar(L::K_FULL + st1), ((c + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
       // slot 0: PV(u), then S(u+1)
       if (n0) {
         if (!wait_bounded(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
-        issue_pv<D>(tmem, sbase, 0, st, !first0);
+        issue_pv<D>(tO0, tS0, v_lo0 + st * kStageLo, !first0);
         mma_commit(bar(L::O_FREE + 0));
         first0 = false;
       }
       if (m0) {
         if (!wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
-        issue_s<D>(tmem, sbase, 0, st1);
+        issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
         mma_commit(bar(L::S_FULL + 0));
         ++s_cnt0;
       }
@@ -380,7 +394,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (n1) {
         if (!wait_bounded(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
-        issue_pv<D>(tmem, sbase, 1, st, !first1);
+        issue_pv<D>(tO1, tS1, v_lo0 + st * kStageLo, !first1);
         mma_commit(bar(L::O_FREE + 1));
         first1 = false;
       }
@@ -388,7 +402,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         if (s_cnt1 > 0 &&
             !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
-        issue_s<D>(tmem, sbase, 1, st1);
+        issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);
         mma_commit(bar(L::S_FULL + 1));
         ++s_cnt1;
       }
@@ -399,7 +413,6 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         if (it.valid1) mma_commit(bar(L::Q_EMPTY + 1));
       }
     }
-    kv_cnt += ns;
   }
   // Every MMA this thread issued completes before tensor memory is freed.
   mma_commit(bar(L::DONE));
@@ -553,13 +566,17 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     const Item it = decode_item(a, x);
     if (slot == 1 && !it.valid1) continue;
     const int ns = n_steps(a, it);
-    int u_last = ns - 1;
-    while (u_last > 0 && !needs(a, it, slot, step_tile(a, it, u_last))) --u_last;
+    // the slot's last step: the item's last one, or the one before it when
+    // the slot does not need the last key tile (the second tile of a causal
+    // pair in a one-chunk item)
+    const int u_last = (ns > 1 && !needs(a, it, slot, last_tile(a, it))) ? ns - 2 : ns - 1;
+    StepCursor cur;
+    cur.init(a, it);
 
     RowState st{-INFINITY, 0.0f, 0.0f};
     bool first = true;
-    for (int u = 0; u < ns; ++u) {
-      const int kt = step_tile(a, it, u);
+    for (int u = 0; u < ns; ++u, cur.next()) {
+      const int kt = cur.kt;
       if (!needs(a, it, slot, kt)) continue;
       if (!wait_warp(bar(L::S_FULL + slot), n & 1, abort_flag, a)) return;
       tc_fence_after();
