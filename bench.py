@@ -222,6 +222,42 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------- GPU arm
+def measure_merge(ra, w, flush, stream, steps: int = 20):
+    """Time ra_merge_partials (the log-sum-exp merge of per-chunk partials)
+    on n = P bf16 partials of the workload's output shape.  It streams its
+    inputs once, so it is measured against HBM bandwidth: algorithmic bytes =
+    n*(B*S*H*D*2 + B*H*S*4) read + B*S*H*D*2 + B*H*S*4 written."""
+    import torch
+
+    n = w.P
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1)
+    o_parts = torch.randn((n, w.B, w.S, w.H, w.D), generator=g, device="cuda").to(torch.bfloat16)
+    lse_parts = torch.randn((n, w.B, w.H, w.S), generator=g, device="cuda")
+    out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        ra.ra_merge_partials(o_parts, lse_parts, out=out, lse=lse, stream=stream)
+    ts = []
+    for _ in range(steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ra.ra_merge_partials(o_parts, lse_parts, out=out, lse=lse, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = statistics.mean(ts)
+    rows = w.B * w.S * w.H
+    nbytes = n * (rows * w.D * 2 + rows * 4) + rows * w.D * 2 + rows * 4
+    peaks, src = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del o_parts, lse_parts
+    return {"kernel": "merge_kernel (ra_merge_partials)", "n_partials": n, "ms": ms,
+            "bytes": nbytes, "bound": "hbm", "achieved": gbs, "peak": float(peaks["hbm_gbs"]),
+            "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "peak_source": f"{src} copy"}
+
+
 def run_ours(args):
     import torch
 
@@ -307,6 +343,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in e2e_evs[1:])
 
+    merge = None if args.no_merge else measure_merge(ra, w, flush, stream)
+
     # slowest rank decides
     if ws > 1:
         import torch.distributed as dist
@@ -350,6 +388,7 @@ def run_ours(args):
             "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms),
                           "max": max(kernel_ms)},
             "kernel_sha": kernel_sha(),
+            "merge": merge,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -367,6 +406,7 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-merge", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
