@@ -122,6 +122,21 @@ int ra_version(void);
  */
 void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
 
+/*
+ * MMA issue order of ra_fwd (no counterpart on the pages; an implementation
+ * choice of this library).  The probabilities P_i of a query tile are kept in
+ * tensor memory over the columns of the score tile S_i that produced them.
+ * By default (strict == 0) the next S_i = Q_i K^T is issued right behind
+ * O_i += P_i V from the same thread, relying on the tensor pipe executing one
+ * thread's MMAs in issue order (as an in-order pipe does); this keeps the
+ * pipe full.  With strict != 0 the issuing thread waits for that PV to
+ * complete before S_i is rewritten, the ordering the PTX ISA guarantees for
+ * MMAs on different accumulators, at the cost of a pipe drain per tile.  Both
+ * orders compute the same arithmetic; the test-suite checks that their
+ * outputs are bit-identical.  Applies to launches made after the call.
+ */
+void ra_set_mma_order(int strict);
+
 /* Drop cached tensor maps and device queries (no device memory is held). */
 void ra_shutdown(void);
 

@@ -19,7 +19,7 @@ import ctypes
 import os
 
 __all__ = ["ra_fwd", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
-           "ra_debug_set_fault", "ra_shutdown", "ra_version", "RaError", "library_path",
+           "ra_debug_set_fault", "ra_set_mma_order", "ra_shutdown", "ra_version", "RaError", "library_path",
            "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT"]
 
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = 0, 1, 2, 3, 4
@@ -29,7 +29,8 @@ _LIB_PATH = os.path.join(_HERE, "libringattn.so")
 _lib = None
 
 EXPORTS = ("ra_fwd", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
-           "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_shutdown")
+           "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_set_mma_order",
+           "ra_shutdown")
 
 
 class RaError(RuntimeError):
@@ -66,6 +67,8 @@ def _load():
     lib.ra_version.restype = i
     lib.ra_debug_set_fault.argtypes = [ctypes.c_longlong, i]
     lib.ra_debug_set_fault.restype = None
+    lib.ra_set_mma_order.argtypes = [i]
+    lib.ra_set_mma_order.restype = None
     lib.ra_shutdown.argtypes = []
     lib.ra_shutdown.restype = None
     _lib = lib
@@ -171,6 +174,12 @@ def ra_get_last_device_status(stream=None) -> int:
 
 def ra_debug_set_fault(timeout_ns: int, skip_value_load: bool) -> None:
     _load().ra_debug_set_fault(int(timeout_ns), int(bool(skip_value_load)))
+
+
+def ra_set_mma_order(strict: bool) -> None:
+    """Strict (wait for each PV before rewriting S) or default in-order MMA
+    issue for subsequent ra_fwd launches; see include/ringattn.h."""
+    _load().ra_set_mma_order(int(bool(strict)))
 
 
 def ra_shutdown() -> None:

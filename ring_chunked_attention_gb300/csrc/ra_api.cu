@@ -24,6 +24,7 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
 std::mutex g_mu;
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 int g_skip_value_load = 0;
+int g_strict_mma_order = 0;
 
 // per-device facts, queried once
 struct DeviceInfo {
@@ -201,6 +202,7 @@ ra_status ra_fwd(const void* q, const void* k, const void* v, void* out, float* 
     std::lock_guard<std::mutex> lock(g_mu);
     a.timeout_ns = g_timeout_ns;
     a.skip_value_load = g_skip_value_load;
+    a.strict_mma_order = g_strict_mma_order;
   }
   const int grid = a.n_items < dev->sms ? a.n_items : dev->sms;
   cudaError_t e = ra::launch_fwd(D, tq, tk, tv, a, grid, static_cast<cudaStream_t>(stream));
@@ -261,12 +263,18 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load) {
   g_skip_value_load = skip_value_load ? 1 : 0;
 }
 
+void ra_set_mma_order(int strict) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_strict_mma_order = strict ? 1 : 0;
+}
+
 void ra_shutdown(void) {
   std::lock_guard<std::mutex> lock(g_mu);
   for (auto& e : g_maps) e.used = false;
   for (auto& d : g_dev) d = DeviceInfo{};
   g_timeout_ns = kDefaultTimeoutNs;
   g_skip_value_load = 0;
+  g_strict_mma_order = 0;
 }
 
 }  // extern "C"

@@ -275,9 +275,13 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 // ---------------------------------------------------------------- MMA issuer
 // Issue order per key/value step u, for each query slot in turn:
 //   O_i += P_i(u) V(u)          once the softmax has written P_i(u)
-//   S_i(u+1) = Q_i K(u+1)^T     once that PV has completed (P_i aliases S_i)
+//   S_i(u+1) = Q_i K(u+1)^T     right behind it
 // so each slot's chain (softmax -> PV -> next S) runs independently of the
 // other slot's softmax, and the tensor pipe alternates between the two.
+// S_i(u+1) overwrites the columns that hold P_i(u), which the PV just issued
+// reads.  The default order relies on the tensor pipe executing this thread's
+// MMAs in issue order; the strict order (FwdArgs::strict_mma_order) waits for
+// the PV to complete first, which drains the pipe once per tile.
 // A tcgen05.mma issue blocks for about the MMA's own execution time, so the
 // issuing thread keeps the work between consecutive MMAs to a few integer
 // operations: descriptors are precomputed halves plus immediate offsets, and
@@ -384,7 +388,8 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         first0 = false;
       }
       if (m0) {
-        if (!wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+        if (a.strict_mma_order &&
+            !wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
         issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
         mma_commit(bar(L::S_FULL + 0));
@@ -399,7 +404,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         first1 = false;
       }
       if (m1) {
-        if (s_cnt1 > 0 &&
+        if (a.strict_mma_order && s_cnt1 > 0 &&
             !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
         issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);

@@ -30,6 +30,7 @@ struct FwdArgs {
   float scale_log2;      // scale * log2(e)
   unsigned long long timeout_ns;
   int skip_value_load;   // failure-path test hook
+  int strict_mma_order;  // 1: wait for O_i += P_i V to complete before S_i is rewritten
 };
 
 // status word bits

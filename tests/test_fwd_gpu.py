@@ -183,3 +183,26 @@ def test_stream_argument_is_used(ralib, cuda_ok, oracle_mod):
     s.synchronize()
     o_ref, l_ref = oracle_mod.attn_direct(q, k, v, True, w.scale)
     assert_parity(compare(out, lse, o_ref, l_ref), "side stream")
+
+
+@pytest.mark.parametrize("name", ["gqa_s16384", "d64_s32768", "small"])
+def test_default_mma_order_is_bit_identical_to_strict_order(ralib, cuda_ok, name):
+    """The default issue order puts the next S MMA right behind the PV MMA
+    that reads the columns it overwrites (relying on in-order execution of one
+    thread's MMAs); the strict order waits for the PV to complete first.  Same
+    arithmetic, so any reordering hazard would show up as a difference."""
+    w = WORKLOADS[name] if name in WORKLOADS else Workload("small", 2, 8, 2, 2048, 128, 4, True)
+    q, k, v = make_inputs(w, seed=43)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    outs = []
+    try:
+        for strict in (True, False, False):
+            ralib.ra_set_mma_order(strict)
+            o, l = ralib.ra_fwd(qd, kd, vd, P=w.P, causal=w.causal)
+            torch.cuda.synchronize()
+            assert ralib.ra_get_last_device_status() == 0
+            outs.append((o, l))
+    finally:
+        ralib.ra_set_mma_order(False)
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
