@@ -64,6 +64,9 @@ def _load():
                                       ctypes.c_double, i64p, ctypes.c_int64,
                                       f64p, f64p, i]
         lib.ora_attn_ring.restype = i
+        lib.ora_attn_block.argtypes = [u16p, u16p, u16p, i, i, i, i, i, i, ctypes.c_longlong,
+                                       ctypes.c_longlong, i, ctypes.c_double, f64p, f64p]
+        lib.ora_attn_block.restype = i
         lib.ora_merge.argtypes = [f64p, f64p, i, i, i, i, i, f64p, f64p]
         lib.ora_merge.restype = i
         lib.ora_default_threads.argtypes = []
@@ -145,6 +148,25 @@ def attn_ring(q, k, v, P: int, causal: bool, scale: float, rows=None, threads: i
     if rows is None:
         out = out.reshape(B, H, S, D).transpose(0, 2, 1, 3).copy()
         lse = lse.reshape(B, H, S)
+    return out, lse
+
+
+def attn_block(q, k, v, q_pos0: int, k_pos0: int, causal: bool, scale: float):
+    """One ring step: q [B,Sq,H,D] (global rows q_pos0..) against k/v
+    [B,Sk,Hkv,D] (global rows k_pos0..).  Returns out [B,Sq,H,D] and lse
+    [B,H,Sq]; rows with no allowed key give 0 and -inf."""
+    B, Sq, H, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    assert Bk == B and Dk == D and tuple(v.shape) == tuple(k.shape)
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    out = np.empty((B, Sq, H, D), np.float64)
+    lse = np.empty((B, H, Sq), np.float64)
+    rc = _load().ora_attn_block(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                _ptr(vb, ctypes.c_uint16), B, H, Hkv, Sq, Sk, D, int(q_pos0),
+                                int(k_pos0), int(bool(causal)), float(scale),
+                                _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"ora_attn_block failed ({rc})")
     return out, lse
 
 

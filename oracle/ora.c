@@ -21,7 +21,7 @@
  * bf16 bit patterns (uint16) and are widened exactly to double; every
  * arithmetic step below is fp64.
  *
- * Three entry points, written independently of each other:
+ * Four entry points, written independently of each other:
  *   ora_attn_direct -- the two-pass definition above (optionally also the
  *                      normalised weights p_st, for small cases);
  *   ora_attn_ring   -- the same result reached the way the method reaches it:
@@ -31,6 +31,9 @@
  *                      from the ring predecessor), causal chunks j > i hold no
  *                      allowed key, and each chunk's (max, sum, accumulator)
  *                      triple is folded into the running triple;
+ *   ora_attn_block  -- one ring step: a query block against one key/value
+ *                      block at given global positions (the partial that the
+ *                      fold combines);
  *   ora_merge       -- combination of normalised partial results (O_k, lse_k)
  *                      computed over disjoint key sets: the fold above written
  *                      in log-sum-exp form.
@@ -274,6 +277,73 @@ int ora_attn_ring(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                rows, rows ? n_rows : (int64_t)B * H * S,
                out, lse, NULL, 1, 0, 0};
     return run(&J, n_threads);
+}
+
+/*
+ * One ring step: attention of a query block against one key/value block at
+ * given global positions.  q [B,Sq,H,D] holds global rows q_pos0..q_pos0+Sq-1,
+ * k/v [B,Sk,Hkv,D] hold global rows k_pos0..k_pos0+Sk-1; causal keeps key
+ * position <= query position.  out [B,Sq,H,D] = the softmax-weighted mean of
+ * the allowed value rows of this block, lse [B,H,Sq] = ln of the sum of their
+ * exp(scores); a row with no allowed key gets out = 0 and lse = -inf.  This
+ * is the per-block partial that the ring fold (and ora_merge) combines.
+ */
+int ora_attn_block(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                   int B, int H, int Hkv, int Sq, int Sk, int D,
+                   long long q_pos0, long long k_pos0, int causal, double scale,
+                   double *out, double *lse)
+{
+    if (B <= 0 || H <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0 || H % Hkv != 0)
+        return -1;
+    double *x = (double *)malloc(sizeof(double) * (size_t)Sk);
+    if (!x)
+        return -2;
+    const int G = H / Hkv;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int s = 0; s < Sq; ++s) {
+                const int g = h / G;
+                const uint16_t *qr = q + (((int64_t)b * Sq + s) * H + h) * D;
+                double *o = out + (((int64_t)b * Sq + s) * H + h) * D;
+                double *l = lse + ((int64_t)b * H + h) * Sq + s;
+                double M = -INFINITY;
+                int any = 0;
+                for (int t = 0; t < Sk; ++t) {
+                    if (causal && k_pos0 + t > q_pos0 + s) {
+                        x[t] = -INFINITY;
+                        continue;
+                    }
+                    const uint16_t *kr = k + (((int64_t)b * Sk + t) * Hkv + g) * D;
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        acc += widen_bf16(qr[d]) * widen_bf16(kr[d]);
+                    x[t] = scale * acc;
+                    if (x[t] > M)
+                        M = x[t];
+                    any = 1;
+                }
+                for (int d = 0; d < D; ++d)
+                    o[d] = 0.0;
+                if (!any) {
+                    *l = -INFINITY;
+                    continue;
+                }
+                double L = 0.0;
+                for (int t = 0; t < Sk; ++t)
+                    if (x[t] != -INFINITY)
+                        L += exp(x[t] - M);
+                for (int t = 0; t < Sk; ++t) {
+                    if (x[t] == -INFINITY)
+                        continue;
+                    const double w = exp(x[t] - M) / L;
+                    const uint16_t *vr = v + (((int64_t)b * Sk + t) * Hkv + g) * D;
+                    for (int d = 0; d < D; ++d)
+                        o[d] += w * widen_bf16(vr[d]);
+                }
+                *l = M + log(L);
+            }
+    free(x);
+    return 0;
 }
 
 /*

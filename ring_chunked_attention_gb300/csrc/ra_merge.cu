@@ -16,12 +16,33 @@
 
 namespace ra {
 
+// 8 consecutive elements of partial p (16-byte bf16 or 2 x 16-byte fp32
+// loads, streamed: every byte is read exactly once) widened to fp32.
+template <bool kFp32>
+__device__ __forceinline__ void load8(const void* base, long long e0, float (&x)[8]) {
+  if (kFp32) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(base) + e0);
+    const float4 a = __ldcs(src), b = __ldcs(src + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
+    const uint4 a = __ldcs(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + e0));
+    const uint32_t v[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(v[j] << 16);
+      x[2 * j + 1] = __uint_as_float(v[j] & 0xFFFF0000u);
+    }
+  }
+}
+
 template <bool kFp32>
 __global__ void __launch_bounds__(256) merge_kernel(const void* __restrict__ o_parts,
                                                     const float* __restrict__ lse_parts, int n,
                                                     __nv_bfloat16* __restrict__ out,
                                                     float* __restrict__ lse, long long rows, int H,
                                                     int S, int D) {
+  constexpr int kBatch = 4;  // partials whose loads are in flight together
   const int per_row = D / 8;
   const long long units = rows * per_row;
   const long long o_stride = rows * (long long)D;  // elements per partial
@@ -35,6 +56,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const void* __restrict__ o_p
     const int s = (int)(bs % S);
     const long long b = bs / S;
     const long long li = (b * H + h) * S + s;  // [B,H,S] order
+    const long long e_row = row * D + cpart * 8;
 
     float M = -INFINITY;
     for (int p = 0; p < n; ++p) M = fmaxf(M, __ldg(lse_parts + p * l_stride + li));
@@ -44,26 +66,23 @@ __global__ void __launch_bounds__(256) merge_kernel(const void* __restrict__ o_p
       float Z = 0.0f;
       for (int p = 0; p < n; ++p) Z += expf(__ldg(lse_parts + p * l_stride + li) - M);
       L = M + logf(Z);
-      for (int p = 0; p < n; ++p) {
-        const float lp = __ldg(lse_parts + p * l_stride + li);
-        if (lp == -INFINITY) continue;
-        const float wgt = expf(lp - L);
-        const long long e0 = p * o_stride + row * D + cpart * 8;
-        if (kFp32) {
-          const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(o_parts) + e0);
-          const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
-          acc[0] += wgt * x0.x; acc[1] += wgt * x0.y; acc[2] += wgt * x0.z; acc[3] += wgt * x0.w;
-          acc[4] += wgt * x1.x; acc[5] += wgt * x1.y; acc[6] += wgt * x1.z; acc[7] += wgt * x1.w;
-        } else {
-          const uint4 x = __ldg(reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(o_parts) + e0));
-          const uint32_t v[4] = {x.x, x.y, x.z, x.w};
+      for (int p0 = 0; p0 < n; p0 += kBatch) {
+        float x[kBatch][8];
+        float wgt[kBatch];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[2 * j] += wgt * __uint_as_float(v[j] << 16);
-            acc[2 * j + 1] += wgt * __uint_as_float(v[j] & 0xFFFF0000u);
-          }
+        for (int q = 0; q < kBatch; ++q) {
+          const int p = p0 + q;
+          const float lp = p < n ? __ldg(lse_parts + p * l_stride + li) : -INFINITY;
+          wgt[q] = lp == -INFINITY ? 0.0f : expf(lp - L);  // an empty partial adds nothing
+          if (lp != -INFINITY) load8<kFp32>(o_parts, p * o_stride + e_row, x[q]);
+          else
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[q][j] = 0.0f;
         }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] += wgt[q] * x[q][j];
       }
     }
     uint32_t packed[4];
@@ -72,8 +91,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const void* __restrict__ o_p
       __nv_bfloat162 t = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
       packed[j] = *reinterpret_cast<uint32_t*>(&t);
     }
-    *reinterpret_cast<uint4*>(out + row * D + cpart * 8) =
-        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    *reinterpret_cast<uint4*>(out + e_row) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     if (lse && cpart == 0) lse[li] = L;
   }
 }

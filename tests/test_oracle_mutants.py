@@ -29,6 +29,10 @@ MUTANTS = {
     "value_row_off_by_one": [("return J->v + (((int64_t)b * J->S + t)",
                               "return J->v + (((int64_t)b * J->S + (t + 1) % J->S)")],
     "merge_weight_uses_max": [("double w = exp(lp - L);", "double w = exp(lp - M);")],
+    "block_ignores_key_offset": [("if (causal && k_pos0 + t > q_pos0 + s) {",
+                                  "if (causal && t > q_pos0 + s) {")],
+    "block_empty_row_not_zeroed": [("                if (!any) {\n                    *l = -INFINITY;",
+                                    "                if (!any) {\n                    o[0] = 1.0;\n                    *l = -INFINITY;")],
     "ring_skips_last_chunk": [("for (int step = 0; step < J->P; ++step)",
                                "for (int step = 0; step < J->P - (J->P > 1); ++step)")],
 }

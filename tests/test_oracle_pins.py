@@ -331,3 +331,50 @@ def test_rejects_bad_shapes(oracle_mod):
     q, k, v = _rand(1, 10, 2, 2, 4)
     with pytest.raises(ValueError):
         oracle_mod.attn_ring(q, k, v, 3, False, 1.0)  # S % P != 0
+
+
+# -------------------------------------------------------------- ring block --
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_over_whole_sequence_is_direct(oracle_mod, causal):
+    q, k, v = _rand(2, 48, 4, 2, 8, seed=37)
+    od, ld = oracle_mod.attn_direct(q, k, v, causal, 0.3)
+    ob, lb = oracle_mod.attn_block(q, k, v, 0, 0, causal, 0.3)
+    np.testing.assert_allclose(ob, od, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lb, ld, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_of_blocks_merges_to_direct(oracle_mod, causal):
+    """Rank i holds query chunk i; at ring step t it receives key/value chunk
+    j = (i - t) mod P and computes that block's partial; merging the P
+    partials gives exact attention over all keys."""
+    B, S, H, Hkv, D, P = 1, 60, 2, 1, 8, 4
+    C = S // P
+    q, k, v = _rand(B, S, H, Hkv, D, seed=41, sq=2.0)
+    od, ld = oracle_mod.attn_direct(q, k, v, causal, 0.45)
+    for i in range(P):
+        qi = q[:, i * C:(i + 1) * C]
+        parts = [oracle_mod.attn_block(qi, k[:, j * C:(j + 1) * C], v[:, j * C:(j + 1) * C],
+                                       i * C, j * C, causal, 0.45)
+                 for j in [(i - t) % P for t in range(P)]]
+        om, lm = oracle_mod.merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        np.testing.assert_allclose(om, od[:, i * C:(i + 1) * C], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lm, ld[:, :, i * C:(i + 1) * C], rtol=0, atol=1e-12)
+
+
+def test_block_in_the_future_is_empty(oracle_mod):
+    q, k, v = _rand(1, 16, 2, 2, 8, seed=43)
+    ob, lb = oracle_mod.attn_block(q, k, v, 0, 16, True, 0.5)  # all keys after all queries
+    assert (ob == 0).all() and np.isneginf(lb).all()
+    ob, lb = oracle_mod.attn_block(q, k, v, 0, 16, False, 0.5)  # non-causal: everything allowed
+    assert np.isfinite(lb).all()
+
+
+def test_block_offsets_on_golden_fixture(oracle_mod):
+    """Query rows 1..2 of the powers-of-two fixture, given as a block at
+    position 1 against all keys at position 0, reproduce the fixture's rows."""
+    q, k, v, scale, cases = _parse_golden(os.path.join(GOLDEN, "powers_of_two.txt"))
+    for c in cases:
+        ob, lb = oracle_mod.attn_block(_bf16(q[:, 1:]), _bf16(k), _bf16(v), 1, 0, c["causal"], scale)
+        np.testing.assert_allclose(ob, c["out"][:, 1:], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lb, c["lse"][:, :, 1:], rtol=0, atol=1e-12)
