@@ -78,6 +78,30 @@ ra_status ra_fwd(const void* q, const void* k, const void* v, void* out, float* 
                  int Hkv, int S, int D, int P, int causal, float scale, void* stream);
 
 /*
+ * ra_fwd_block -- one ring step: attention of a query block against one
+ * key/value block at given global sequence positions, as a normalised
+ * partial result.  This is what a ring rank computes on the block it has
+ * just received (same page, table "Die fünf verschmolzenen Kerne", row Ring
+ * Attention); ra_merge_partials then folds the partials of all blocks into the
+ * exact result.
+ *
+ *   q    [B, Sq, H,   D] bf16: global query rows q_pos0 .. q_pos0+Sq-1
+ *   k, v [B, Sk, Hkv, D] bf16: global key rows   k_pos0 .. k_pos0+Sk-1
+ *   out  [B, Sq, H,   D] bf16, written: softmax over this block's allowed keys
+ *        (causal: key position <= query position) applied to v
+ *   lse  [B, H, Sq]      fp32, written: ln sum over those keys of exp(x_t);
+ *        may be NULL
+ *   A row with no allowed key in the block gets out = 0 and lse = -inf (it
+ *   contributes nothing to a merge).
+ *   supported: D in {64, 128}; Sq, Sk, q_pos0, k_pos0 multiples of 128;
+ *   scale >= 0; q_pos0, k_pos0 >= 0 (RA_ERR_INVALID_ARG otherwise).
+ * Same pointer, alignment, stream and error rules as ra_fwd.
+ */
+ra_status ra_fwd_block(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                       int H, int Hkv, int Sq, int Sk, int D, long long q_pos0, long long k_pos0,
+                       int causal, float scale, void* stream);
+
+/*
  * ra_merge_partials -- combine n normalised partial attention results that
  * were computed over disjoint key sets (for instance one per ring chunk) into
  * the result over their union: the online-softmax fold of the same page's

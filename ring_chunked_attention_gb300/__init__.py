@@ -18,7 +18,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["ra_fwd", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+__all__ = ["ra_fwd", "ra_fwd_block", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
            "ra_debug_set_fault", "ra_set_mma_order", "ra_shutdown", "ra_version", "RaError", "library_path",
            "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT"]
 
@@ -28,7 +28,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libringattn.so")
 _lib = None
 
-EXPORTS = ("ra_fwd", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
            "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_set_mma_order",
            "ra_shutdown")
 
@@ -55,6 +55,9 @@ def _load():
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.ra_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.ra_fwd.restype = i
+    ll = ctypes.c_longlong
+    lib.ra_fwd_block.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ll, ll, i, f, vp]
+    lib.ra_fwd_block.restype = i
     lib.ra_merge_partials.argtypes = [vp, i, vp, i, vp, vp, i, i, i, i, vp]
     lib.ra_merge_partials.restype = i
     lib.ra_get_last_device_status.argtypes = [vp]
@@ -128,6 +131,36 @@ def ra_fwd(q, k, v, *, P: int, causal: bool, scale: float | None = None, out=Non
                       None if lse is None else lse.data_ptr(), B, H, Hkv, S, D, int(P),
                       int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(code, "ra_fwd")
+    return out, lse
+
+
+def ra_fwd_block(q, k, v, *, q_pos0: int, k_pos0: int, causal: bool, scale: float | None = None,
+                 out=None, lse=None, want_lse: bool = True, stream=None):
+    """One ring step: ``q`` [B,Sq,H,D] (global rows q_pos0..) against ``k``/``v``
+    [B,Sk,Hkv,D] (global rows k_pos0..).  Returns the normalised partial
+    ``(out [B,Sq,H,D] bf16, lse [B,H,Sq] fp32)``; rows with no allowed key get
+    0 and -inf."""
+    import torch
+
+    lib = _load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{n} must be a contiguous 4-D bf16 CUDA tensor")
+    B, Sq, H, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B,Sk,Hkv,D] matching q's B and D")
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    code = lib.ra_fwd_block(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            None if lse is None else lse.data_ptr(), B, H, Hkv, Sq, Sk, D,
+                            int(q_pos0), int(k_pos0), int(bool(causal)), float(scale),
+                            _stream_ptr(stream))
+    _check(code, "ra_fwd_block")
     return out, lse
 
 

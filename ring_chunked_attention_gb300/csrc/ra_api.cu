@@ -143,31 +143,24 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" {
 
-ra_status ra_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
-                 int Hkv, int S, int D, int P, int causal, float scale, void* stream) {
-  if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || P <= 0) return RA_ERR_INVALID_ARG;
-  if (H % Hkv != 0 || S % P != 0) return RA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return RA_ERR_INVALID_ARG;
-  if (scale < 0.0f) return RA_ERR_UNSUPPORTED;
-  if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
-  const int C = S / P;
-  if (C % 128 != 0) return RA_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_UNSUPPORTED;
-  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return RA_ERR_UNSUPPORTED;
-  const long long rows = (long long)B * S;
-  if (rows >= (1ll << 31) || (long long)B * H * (S / 128) >= (1ll << 31))
-    return RA_ERR_UNSUPPORTED;
+}  // extern "C"
 
+namespace {
+
+// Shared tail of ra_fwd and ra_fwd_block: device check, tensor maps, work
+// decomposition, launch.  Arguments are already validated.
+ra_status launch_attention(const void* q, const void* k, const void* v, void* out, float* lse,
+                           int B, int H, int Hkv, int Sq, int Sk, int D, int P, int causal,
+                           float scale, int block, int q_tile0, int k_tile0, void* stream) {
   DeviceInfo* dev = nullptr;
   ra_status st = device_info(&dev);
   if (st != RA_OK) return st;
   if (!dev->sm103) return RA_ERR_UNSUPPORTED;
 
   CUtensorMap tq, tk, tv;
-  if ((st = tensor_map(q, rows, H, D, &tq)) != RA_OK) return st;
-  if ((st = tensor_map(k, rows, Hkv, D, &tk)) != RA_OK) return st;
-  if ((st = tensor_map(v, rows, Hkv, D, &tv)) != RA_OK) return st;
+  if ((st = tensor_map(q, (long long)B * Sq, H, D, &tq)) != RA_OK) return st;
+  if ((st = tensor_map(k, (long long)B * Sk, Hkv, D, &tk)) != RA_OK) return st;
+  if ((st = tensor_map(v, (long long)B * Sk, Hkv, D, &tv)) != RA_OK) return st;
 
   ra::FwdArgs a;
   std::memset(&a, 0, sizeof a);
@@ -177,17 +170,24 @@ ra_status ra_fwd(const void* q, const void* k, const void* v, void* out, float* 
   a.B = B;
   a.H = H;
   a.Hkv = Hkv;
-  a.S = S;
+  a.S = Sq;
+  a.Sk = Sk;
   a.P = P;
   a.causal = causal ? 1 : 0;
-  a.tiles = S / 128;
-  a.tpc = C / 128;
+  a.tiles = Sq / 128;
+  a.tiles_k = Sk / 128;
+  a.tpc = block ? a.tiles_k : Sq / P / 128;
+  a.block = block;
+  a.q_tile0 = q_tile0;
+  a.k_tile0 = k_tile0;
   const int G = H / Hkv;
+  // two consecutive query tiles pair up only inside one ring chunk
+  const bool pair_tiles = block ? (a.tiles % 2 == 0) : (a.tpc % 2 == 0);
   if (G % 2 == 0) {
     a.mode = ra::MODE_HEADS;
     a.groups = B * Hkv * (G / 2);
     a.nq = a.tiles;
-  } else if (a.tpc % 2 == 0) {
+  } else if (pair_tiles) {
     a.mode = ra::MODE_QTILES;
     a.groups = B * H;
     a.nq = a.tiles / 2;
@@ -208,6 +208,48 @@ ra_status ra_fwd(const void* q, const void* k, const void* v, void* out, float* 
   cudaError_t e = ra::launch_fwd(D, tq, tk, tv, a, grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ra_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+                 int Hkv, int S, int D, int P, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || P <= 0) return RA_ERR_INVALID_ARG;
+  if (H % Hkv != 0 || S % P != 0) return RA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return RA_ERR_INVALID_ARG;
+  if (scale < 0.0f) return RA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
+  if ((S / P) % 128 != 0) return RA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_UNSUPPORTED;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return RA_ERR_UNSUPPORTED;
+  if ((long long)B * S >= (1ll << 31) || (long long)B * H * (S / 128) >= (1ll << 31))
+    return RA_ERR_UNSUPPORTED;
+  return launch_attention(q, k, v, out, lse, B, H, Hkv, S, S, D, P, causal, scale, 0, 0, 0,
+                          stream);
+}
+
+ra_status ra_fwd_block(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                       int H, int Hkv, int Sq, int Sk, int D, long long q_pos0, long long k_pos0,
+                       int causal, float scale, void* stream) {
+  if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return RA_ERR_INVALID_ARG;
+  if (H % Hkv != 0 || q_pos0 < 0 || k_pos0 < 0) return RA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return RA_ERR_INVALID_ARG;
+  if (scale < 0.0f) return RA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
+  if (Sq % 128 != 0 || Sk % 128 != 0 || q_pos0 % 128 != 0 || k_pos0 % 128 != 0)
+    return RA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_UNSUPPORTED;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return RA_ERR_UNSUPPORTED;
+  if ((long long)B * Sq >= (1ll << 31) || (long long)B * Sk >= (1ll << 31) ||
+      (long long)B * H * (Sq / 128) >= (1ll << 31) || q_pos0 / 128 + Sq / 128 >= (1ll << 30) ||
+      k_pos0 / 128 + Sk / 128 >= (1ll << 30))
+    return RA_ERR_UNSUPPORTED;
+  return launch_attention(q, k, v, out, lse, B, H, Hkv, Sq, Sk, D, 1, causal, scale, 1,
+                          (int)(q_pos0 / 128), (int)(k_pos0 / 128), stream);
 }
 
 ra_status ra_merge_partials(const void* o_parts, int o_is_fp32, const float* lse_parts, int n,

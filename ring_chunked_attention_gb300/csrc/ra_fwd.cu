@@ -125,6 +125,11 @@ __device__ __forceinline__ int qmax_of(const Item& it) {
 }
 
 __device__ __forceinline__ int n_steps(const FwdArgs& a, const Item& it) {
+  if (a.block) {  // key tiles 0.. of the block, up to the pair's last diagonal
+    if (!a.causal) return a.tiles_k;
+    const int n = a.q_tile0 + qmax_of(it) - a.k_tile0 + 1;
+    return n < 0 ? 0 : (n > a.tiles_k ? a.tiles_k : n);
+  }
   return a.causal ? qmax_of(it) + 1 : a.tiles;
 }
 
@@ -138,6 +143,13 @@ struct StepCursor {
   int j;     // current chunk
   int tpc, P;
   __device__ __forceinline__ void init(const FwdArgs& a, const Item& it) {
+    if (a.block) {  // one block: its key tiles in ascending order
+      tpc = P = 1;
+      j = 0;
+      kt = 0;
+      left = 1 << 30;
+      return;
+    }
     tpc = a.tpc;
     P = a.P;
     j = it.qt[0] / a.tpc;
@@ -157,6 +169,7 @@ struct StepCursor {
 
 // Key tile of the item's last step.
 __device__ __forceinline__ int last_tile(const FwdArgs& a, const Item& it) {
+  if (a.block) return n_steps(a, it) - 1;
   const int ci = it.qt[0] / a.tpc;
   if (a.causal) return ci > 0 ? a.tpc - 1 : qmax_of(it);
   const int j = (ci + 1 == a.P) ? 0 : ci + 1;
@@ -165,7 +178,12 @@ __device__ __forceinline__ int last_tile(const FwdArgs& a, const Item& it) {
 
 __device__ __forceinline__ bool needs(const FwdArgs& a, const Item& it, int slot, int kt) {
   if (slot == 1 && !it.valid1) return false;
-  return !a.causal || kt <= it.qt[slot];
+  return !a.causal || a.k_tile0 + kt <= a.q_tile0 + it.qt[slot];
+}
+
+// The key tile is the query tile's diagonal (causal only): mask keys past the row.
+__device__ __forceinline__ bool is_diag(const FwdArgs& a, const Item& it, int slot, int kt) {
+  return a.causal && a.k_tile0 + kt == a.q_tile0 + it.qt[slot];
 }
 
 // Bounded wait on one mbarrier phase (single thread).
@@ -224,6 +242,8 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
     const int x = item_index(k);
     if (x >= a.n_items) continue;
     const Item it = decode_item(a, x);
+    const int ns = n_steps(a, it);
+    if (ns == 0) continue;  // every key of the block is in the future of every row
 #pragma unroll
     for (int slot = 0; slot < 2 && ok; ++slot) {
       if (slot == 1 && !it.valid1) continue;
@@ -238,14 +258,13 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
                     kb * 64, it.h[slot], it.b * a.S + it.qt[slot] * kBM, pol_q);
       ++q_cnt[slot];
     }
-    const int ns = n_steps(a, it);
     StepCursor cur;
     cur.init(a, it);
     for (int u = 0; u < ns && ok; ++u, cur.next()) {
       const int kt = cur.kt;
       const int st = kv_cnt % L::NS;
       const uint32_t ph = (kv_cnt / L::NS) & 1;
-      const int row = it.b * a.S + kt * kBN;
+      const int row = it.b * a.Sk + kt * kBN;
       if (!wait_bounded(bar(L::K_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
       mbar_arrive_expect_tx(bar(L::K_FULL + st), L::TILE);
       for (int kb = 0; kb < L::DK; ++kb)
@@ -335,13 +354,14 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     const int x = item_index(k);
     if (x >= a.n_items) continue;
     const Item it = decode_item(a, x);
+    const int ns = n_steps(a, it);
+    if (ns == 0) continue;
     if (!wait_bounded(bar(L::Q_FULL + 0), q_cnt0 & 1, abort_flag, a)) break;
     ++q_cnt0;
     if (it.valid1) {
       if (!wait_bounded(bar(L::Q_FULL + 1), q_cnt1 & 1, abort_flag, a)) break;
       ++q_cnt1;
     }
-    const int ns = n_steps(a, it);
     StepCursor nxt;  // the step whose S MMAs are issued next
     nxt.init(a, it);
     // prologue: S(0) for both slots
@@ -571,6 +591,16 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     const Item it = decode_item(a, x);
     if (slot == 1 && !it.valid1) continue;
     const int ns = n_steps(a, it);
+    if (ns == 0 || !needs(a, it, slot, 0)) {
+      // block mode only: no key of the block is allowed for these rows
+      const int srow = it.qt[slot] * kBM + r;
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                             (((size_t)it.b * a.S + srow) * a.H + it.h[slot]) * D);
+#pragma unroll 1
+      for (int j = 0; j < D / 8; ++j) orow[j] = make_uint4(0, 0, 0, 0);
+      if (a.lse) a.lse[((size_t)it.b * a.H + it.h[slot]) * a.S + srow] = -INFINITY;
+      continue;
+    }
     // the slot's last step: the item's last one, or the one before it when
     // the slot does not need the last key tile (the second tile of a causal
     // pair in a one-chunk item)
@@ -585,7 +615,7 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (!needs(a, it, slot, kt)) continue;
       if (!wait_warp(bar(L::S_FULL + slot), n & 1, abort_flag, a)) return;
       tc_fence_after();
-      if (a.causal && kt == it.qt[slot])
+      if (is_diag(a, it, slot, kt))
         softmax_tile<D, true>(tS, tO, r, c, first, st);
       else
         softmax_tile<D, false>(tS, tO, r, c, first, st);

@@ -19,11 +19,16 @@ struct FwdArgs {
   void* out;             // bf16 [B,S,H,D]
   float* lse;            // fp32 [B,H,S] or nullptr
   unsigned int* status;  // this device's sticky status word
-  int B, H, Hkv, S, P;
+  int B, H, Hkv, S, P;   // S: query rows per batch entry
+  int Sk;                // key rows per batch entry (== S for the ring-chunked forward)
   int causal;
   int mode;              // PairMode
-  int tiles;             // S / 128
+  int tiles;             // S / 128 (query tiles)
+  int tiles_k;           // Sk / 128 (key tiles)
   int tpc;               // 128-row tiles per chunk (S / P / 128)
+  int block;             // 0: ring-chunked forward over P chunks; 1: one query block
+                         //    against one key/value block at the offsets below
+  int q_tile0, k_tile0;  // block mode: global 128-row tile index of query / key row 0
   int groups;            // work items per query-tile index
   int nq;                // query-tile indices
   int n_items;           // groups * nq

@@ -77,3 +77,19 @@ def test_merge_validation_rejects_before_launch(ralib, kw, code):
     rc = lib.ra_merge_partials(a["o"], 0, a["l"], a["n"], a["out"], a["lse"], a["B"], a["H"],
                                a["S"], a["D"], None)
     assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(Sk=0), 1), (dict(qp=-128), 1), (dict(kp=-128), 1),
+    (dict(H=3, Hkv=2), 1), (dict(scale=float("nan")), 1),
+    (dict(Sq=200), 2), (dict(Sk=100), 2), (dict(qp=64), 2), (dict(kp=1), 2), (dict(D=32), 2),
+    (dict(scale=-1.0), 2), (dict(o=O + 4), 2),
+])
+def test_block_validation_rejects_before_launch(ralib, kw, code):
+    a = dict(q=Q, k=K, v=V, o=O, l=L, B=1, H=4, Hkv=2, Sq=256, Sk=384, D=128, qp=256, kp=0,
+             causal=1, scale=0.125)
+    a.update(kw)
+    lib = ralib._load()
+    rc = lib.ra_fwd_block(a["q"], a["k"], a["v"], a["o"], a["l"], a["B"], a["H"], a["Hkv"], a["Sq"],
+                          a["Sk"], a["D"], a["qp"], a["kp"], a["causal"], a["scale"], None)
+    assert rc == code
