@@ -265,6 +265,7 @@ ra_status ra_merge_partials(const void* o_parts, int o_is_fp32, const float* lse
   if (st != RA_OK) return st;
   if (!dev->sm103) return RA_ERR_UNSUPPORTED;
   const long long rows = (long long)B * S * H;
+  if (rows >= (1ll << 31)) return RA_ERR_UNSUPPORTED;
   const long long units = rows * (D / 8);
   long long grid = (units + 255) / 256;
   const long long cap = (long long)dev->sms * 8;  // 8 resident 256-thread blocks per SM

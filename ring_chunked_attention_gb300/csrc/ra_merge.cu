@@ -44,18 +44,21 @@ __global__ void __launch_bounds__(256) merge_kernel(const void* __restrict__ o_p
                                                     int S, int D) {
   constexpr int kBatch = 4;  // partials whose loads are in flight together
   const int per_row = D / 8;
+  const int pr_shift = (per_row & (per_row - 1)) == 0 ? __ffs(per_row) - 1 : -1;
   const long long units = rows * per_row;
   const long long o_stride = rows * (long long)D;  // elements per partial
   const long long l_stride = rows;                 // B*H*S == rows
   for (long long w = blockIdx.x * (long long)blockDim.x + threadIdx.x; w < units;
        w += (long long)gridDim.x * blockDim.x) {
-    const long long row = w / per_row;  // [B,S,H] order
-    const int cpart = (int)(w % per_row);
-    const int h = (int)(row % H);
-    const long long bs = row / H;
-    const int s = (int)(bs % S);
-    const long long b = bs / S;
-    const long long li = (b * H + h) * S + s;  // [B,H,S] order
+    // rows < 2^31 (checked on the host): 32-bit index arithmetic
+    const unsigned row32 = (unsigned)(pr_shift >= 0 ? (w >> pr_shift) : w / per_row);  // [B,S,H]
+    const long long row = row32;
+    const int cpart = (int)(w - row * per_row);
+    const unsigned h = row32 % (unsigned)H;
+    const unsigned bs = row32 / (unsigned)H;
+    const unsigned s = bs % (unsigned)S;
+    const unsigned b = bs / (unsigned)S;
+    const long long li = ((long long)b * H + h) * S + s;  // [B,H,S] order
     const long long e_row = row * D + cpart * 8;
 
     float M = -INFINITY;
