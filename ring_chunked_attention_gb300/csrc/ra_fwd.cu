@@ -45,7 +45,19 @@ constexpr int kWarpMma = 9;
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+// Reference-max policy of the online softmax, per head dimension.
+//  D = 128 (tensor-bound): the reference max m is refreshed only when a row's
+//    max grows by more than 2^8 (O is rescaled rarely); the dominant weight is
+//    then 2^(x - m) != 1 and its bf16 rounding would bias O / l, so the row
+//    keeps a second sum of the rounded weights for the output normalisation.
+//  D = 64 (softmax-bound): m always follows the exact running max, so the
+//    dominant weight is exactly 1 and one exact sum normalises both O and lse;
+//    the extra O rescales cost less than the second sum (measured).
+template <int D>
+struct SoftmaxPolicy {
+  static constexpr bool kExactMax = (D == 64);
+  static constexpr float kRescaleThreshold = kExactMax ? 0.0f : 8.0f;  // log2 units
+};
 
 template <int D>
 struct Layout {
@@ -469,7 +481,7 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], int j0, int 
 // p = exp2(x*c - m) for one 32-column chunk; packs bf16 pairs into pk and
 // accumulates both the exact fp32 sum (for lse) and the sum of the rounded
 // values that the PV product consumes (for the output normalisation).
-template <bool DIAG>
+template <bool DIAG, bool kRoundedSum>
 __device__ __forceinline__ void chunk_exp(const uint32_t (&v)[32], int j0, int r, uint64_t c2,
                                           uint64_t negm2, uint64_t& se0, uint64_t& se1,
                                           uint64_t& sr0, uint64_t& sr1, uint32_t (&pk)[16]) {
@@ -482,13 +494,12 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&v)[32], int j0, int r
       p1 = (j0 + j + 1 > r) ? 0.0f : p1;
     }
     const uint32_t pr = pack_bf16x2(p0, p1);
-    const uint64_t prf = ((uint64_t)(pr & 0xFFFF0000u) << 32) | (uint64_t)(pr << 16);
-    if ((j & 2) == 0) {
-      se0 = f2_add(se0, f2_pack(p0, p1));
-      sr0 = f2_add(sr0, prf);
-    } else {
-      se1 = f2_add(se1, f2_pack(p0, p1));
-      sr1 = f2_add(sr1, prf);
+    if ((j & 2) == 0) se0 = f2_add(se0, f2_pack(p0, p1));
+    else se1 = f2_add(se1, f2_pack(p0, p1));
+    if (kRoundedSum) {
+      const uint64_t prf = ((uint64_t)(pr & 0xFFFF0000u) << 32) | (uint64_t)(pr << 16);
+      if ((j & 2) == 0) sr0 = f2_add(sr0, prf);
+      else sr1 = f2_add(sr1, prf);
     }
     pk[j >> 1] = pr;
   }
@@ -526,7 +537,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, fl
   float alpha = 1.0f;
   if (first) {
     st.m = mx;
-  } else if (mx > st.m + kRescaleThreshold) {
+  } else if (mx > st.m + SoftmaxPolicy<D>::kRescaleThreshold) {
     alpha = ex2(st.m - mx);
     st.m = mx;
     st.l_exact *= alpha;
@@ -551,22 +562,23 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, fl
   uint64_t se0 = 0, se1 = 0, sr0 = 0, sr1 = 0;
   uint32_t pk[16];
   tmem_ld32(tS + 32, vb);
-  chunk_exp<DIAG>(va, 0, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(va, 0, r, c2, negm2, se0, se1, sr0, sr1, pk);
   tmem_st16(tS + 0, pk);
   tmem_wait_ld_regs(vb);
   tmem_ld32(tS + 64, va);
-  chunk_exp<DIAG>(vb, 32, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(vb, 32, r, c2, negm2, se0, se1, sr0, sr1, pk);
   tmem_st16(tS + 16, pk);
   tmem_wait_ld_regs(va);
   tmem_ld32(tS + 96, vb);
-  chunk_exp<DIAG>(va, 64, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(va, 64, r, c2, negm2, se0, se1, sr0, sr1, pk);
   tmem_st16(tS + 32, pk);
   tmem_wait_ld_regs(vb);
-  chunk_exp<DIAG>(vb, 96, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(vb, 96, r, c2, negm2, se0, se1, sr0, sr1, pk);
   tmem_st16(tS + 48, pk);
   const uint64_t se = f2_add(se0, se1), sr = f2_add(sr0, sr1);
   st.l_exact += f2_lo(se) + f2_hi(se);
-  st.l_round += f2_lo(sr) + f2_hi(sr);
+  if (SoftmaxPolicy<D>::kExactMax) st.l_round = st.l_exact;  // dominant weight is exactly 1
+  else st.l_round += f2_lo(sr) + f2_hi(sr);
   tmem_wait_st();
 }
 
