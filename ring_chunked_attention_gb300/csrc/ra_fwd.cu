@@ -14,6 +14,11 @@
 //   warps 4-7  the same for query slot 1
 //   warp  8    TMA producer: Q tiles, then K/V tiles into an NS-stage ring
 //   warp  9    MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V
+//   warps 10-11 idle (they complete the producer warpgroup)
+// Registers are split with setmaxnreg: the launch gives every thread 168
+// (three warps per SM sub-partition); the two softmax warpgroups raise theirs
+// to 200 so a thread can hold its whole 128-column score row, the producer
+// warpgroup drops to 104 (2*128*200 + 128*104 = 384*168).
 // A work item is two 128-row query tiles sharing one key/value stream (two
 // heads of one GQA group, or two consecutive tiles of one head), so every
 // K/V tile staged in shared memory feeds two MMAs.
@@ -39,7 +44,10 @@ namespace ra {
 
 __device__ unsigned int g_status_word;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr uint32_t kLaunchRegs = 168, kSoftmaxRegs = 200, kProducerRegs = 104;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kProducerRegs == kThreads * kLaunchRegs,
+              "register split must use exactly the launch allocation");
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 constexpr int kBM = 128;  // query rows per tile
@@ -199,7 +207,7 @@ __device__ __forceinline__ bool is_diag(const FwdArgs& a, const Item& it, int sl
 }
 
 // Bounded wait on one mbarrier phase (single thread).
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        unsigned long long timeout_ns, unsigned int* status) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -515,21 +523,22 @@ struct RowState {
 template <int D, bool DIAG>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, float c, bool first,
                                              RowState& st) {
-  uint32_t va[32], vb[32];
-  // pass 1: row max, one chunk in flight while the previous one is reduced
+  // the whole score row is loaded once (four 32-column loads in flight) and
+  // stays in registers for both passes
+  uint32_t va[32], vb[32], vc[32], vd[32];
   tmem_ld32(tS + 0, va);
-  tmem_wait_ld_regs(va);
   tmem_ld32(tS + 32, vb);
-  float mx = chunk_max<DIAG>(va, 0, r, -INFINITY);
-  tmem_wait_ld_regs(vb);
-  tmem_ld32(tS + 64, va);
-  mx = chunk_max<DIAG>(vb, 32, r, mx);
+  tmem_ld32(tS + 64, vc);
+  tmem_ld32(tS + 96, vd);
   tmem_wait_ld_regs(va);
-  tmem_ld32(tS + 96, vb);
-  mx = chunk_max<DIAG>(va, 64, r, mx);
   tmem_wait_ld_regs(vb);
-  mx = chunk_max<DIAG>(vb, 96, r, mx);
-  tmem_ld32(tS + 0, va);  // pass 2 starts; overlaps the max bookkeeping below
+  tmem_wait_ld_regs(vc);
+  tmem_wait_ld_regs(vd);
+  // pass 1: row max
+  float mx = chunk_max<DIAG>(va, 0, r, -INFINITY);
+  mx = chunk_max<DIAG>(vb, 32, r, mx);
+  mx = chunk_max<DIAG>(vc, 64, r, mx);
+  mx = chunk_max<DIAG>(vd, 96, r, mx);
   mx *= c;
 
   // reference-max update; O is rescaled only when the max grows past the
@@ -543,7 +552,6 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, fl
     st.l_exact *= alpha;
     st.l_round *= alpha;
   }
-  tmem_wait_ld_regs(va);
   if (!first && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -561,19 +569,13 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, fl
   const uint64_t negm2 = f2_pack(-st.m, -st.m);
   uint64_t se0 = 0, se1 = 0, sr0 = 0, sr1 = 0;
   uint32_t pk[16];
-  tmem_ld32(tS + 32, vb);
   chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(va, 0, r, c2, negm2, se0, se1, sr0, sr1, pk);
   tmem_st16(tS + 0, pk);
-  tmem_wait_ld_regs(vb);
-  tmem_ld32(tS + 64, va);
   chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(vb, 32, r, c2, negm2, se0, se1, sr0, sr1, pk);
   tmem_st16(tS + 16, pk);
-  tmem_wait_ld_regs(va);
-  tmem_ld32(tS + 96, vb);
-  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(va, 64, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(vc, 64, r, c2, negm2, se0, se1, sr0, sr1, pk);
   tmem_st16(tS + 32, pk);
-  tmem_wait_ld_regs(vb);
-  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(vb, 96, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(vd, 96, r, c2, negm2, se0, se1, sr0, sr1, pk);
   tmem_st16(tS + 48, pk);
   const uint64_t se = f2_add(se0, se1), sr = f2_add(sr0, sr1);
   st.l_exact += f2_lo(se) + f2_hi(se);
@@ -706,11 +708,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   if (warp < 8) {
+    regs_inc<kSoftmaxRegs>();
     softmax_role<D>(a, sbase, tmem, abort_flag);
-  } else if (warp == kWarpTma) {
-    if ((threadIdx.x & 31) == 0) tma_role<D>(&tm_q, &tm_k, &tm_v, a, sbase, abort_flag);
   } else {
-    if ((threadIdx.x & 31) == 0) mma_role<D>(a, sbase, tmem, abort_flag);
+    regs_dec<kProducerRegs>();
+    if (warp == kWarpTma) {
+      if ((threadIdx.x & 31) == 0) tma_role<D>(&tm_q, &tm_k, &tm_v, a, sbase, abort_flag);
+    } else if (warp == kWarpMma) {
+      if ((threadIdx.x & 31) == 0) mma_role<D>(a, sbase, tmem, abort_flag);
+    }
   }
 
   tc_fence_before();
@@ -730,8 +736,14 @@ template <int D>
 static cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdArgs& args, int grid, cudaStream_t stream) {
   const int smem = Layout<D>::ALLOC;
-  cudaError_t e = cudaFuncSetAttribute(ring_attn_fwd_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // the setmaxnreg split is sized for exactly kLaunchRegs registers per thread
+  // at launch; any other allocation would make setmaxnreg.inc wait forever
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, ring_attn_fwd_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != (int)kLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(ring_attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem);
   if (e != cudaSuccess) return e;
   ring_attn_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
   return cudaGetLastError();
