@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for ring-chunked attention forward.
+"""fp64 CPU oracle for ring-chunked attention (forward, and its gradients).
 
 TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, the smoke check in
 ``__graft_entry__`` and ``bench.py``'s CPU-baseline / reference arm may import
@@ -69,6 +69,12 @@ def _load():
         lib.ora_attn_block.restype = i
         lib.ora_merge.argtypes = [f64p, f64p, i, i, i, i, i, f64p, f64p]
         lib.ora_merge.restype = i
+        lib.ora_attn_bwd.argtypes = [u16p, u16p, u16p, u16p, i, i, i, i, i, i, ctypes.c_double,
+                                     f64p, f64p, f64p, i]
+        lib.ora_attn_bwd.restype = i
+        lib.ora_attn_bwd_dq.argtypes = [u16p, u16p, u16p, u16p, i, i, i, i, i, i, ctypes.c_double,
+                                        i64p, ctypes.c_int64, f64p, i]
+        lib.ora_attn_bwd_dq.restype = i
         lib.ora_default_threads.argtypes = []
         lib.ora_default_threads.restype = i
         _lib = lib
@@ -184,6 +190,41 @@ def merge(o_parts: np.ndarray, lse_parts: np.ndarray):
     if rc != 0:
         raise ValueError(f"ora_merge failed ({rc})")
     return out, lse
+
+
+def attn_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0):
+    """Gradients of ``sum(out * dout)`` for the attention above (the
+    derivative of the definition; see ``ora.c``).  Returns fp64 ``dq``
+    [B,S,H,D], ``dk`` and ``dv`` [B,S,Hkv,D]."""
+    B, S, H, Hkv, D = _shapes(q, k, v)
+    assert tuple(dout.shape) == tuple(q.shape)
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+    dq = np.empty((B, S, H, D), np.float64)
+    dk = np.empty((B, S, Hkv, D), np.float64)
+    dv = np.empty((B, S, Hkv, D), np.float64)
+    rc = _load().ora_attn_bwd(
+        _ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16), _ptr(vb, ctypes.c_uint16),
+        _ptr(db, ctypes.c_uint16), B, H, Hkv, S, D, int(bool(causal)), float(scale),
+        _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
+        int(threads))
+    if rc != 0:
+        raise ValueError(f"ora_attn_bwd failed ({rc})")
+    return dq, dk, dv
+
+
+def attn_bwd_dq(q, k, v, dout, causal: bool, scale: float, rows, threads: int = 0):
+    """``dq`` of selected query rows (flat ids ``(b*H + h)*S + s``), [n, D]."""
+    B, S, H, Hkv, D = _shapes(q, k, v)
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+    rows_a = np.ascontiguousarray(rows, dtype=np.int64)
+    dq = np.empty((len(rows_a), D), np.float64)
+    rc = _load().ora_attn_bwd_dq(
+        _ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16), _ptr(vb, ctypes.c_uint16),
+        _ptr(db, ctypes.c_uint16), B, H, Hkv, S, D, int(bool(causal)), float(scale),
+        _ptr(rows_a, ctypes.c_int64), len(rows_a), _ptr(dq, ctypes.c_double), int(threads))
+    if rc != 0:
+        raise ValueError(f"ora_attn_bwd_dq failed ({rc})")
+    return dq
 
 
 if __name__ == "__main__":  # pragma: no cover

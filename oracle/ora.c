@@ -36,7 +36,11 @@
  *                      fold combines);
  *   ora_merge       -- combination of normalised partial results (O_k, lse_k)
  *                      computed over disjoint key sets: the fold above written
- *                      in log-sum-exp form.
+ *                      in log-sum-exp form;
+ *   ora_attn_bwd    -- gradients of out with respect to q, k and v for a given
+ *   ora_attn_bwd_dq    output gradient (the pages describe no backward pass;
+ *                      this is the derivative of the definition above, see
+ *                      the comment at bwd_row).
  */
 #include <math.h>
 #include <pthread.h>
@@ -393,4 +397,170 @@ int ora_merge(const double *o_parts, const double *lse_parts, int n,
                 lse[li] = L;
             }
     return 0;
+}
+
+/*
+ * Backward pass: the derivative of the definition at the top of this file.
+ * For the loss  sum_{b,s,h,d} out[b,s,h,d] * dout[b,s,h,d]  and one query row
+ * (b, h, s) with KV head g, weights p_t = exp(x_t - M) / L over allowed t:
+ *
+ *   dp_t  = <dout[b,s,h,:], v[b,t,g,:]>            (d loss / d p_t)
+ *   delta = sum_t p_t dp_t                        (= <dout, out> of the row)
+ *   ds_t  = p_t (dp_t - delta)                    (softmax Jacobian applied)
+ *   dq[b,s,h,:]  = scale * sum_t ds_t k[b,t,g,:]
+ *   dk[b,t,g,:] += scale * ds_t q[b,s,h,:]        (summed over rows and over
+ *   dv[b,t,g,:] += p_t dout[b,s,h,:]               the query heads of group g)
+ *
+ * Every step in fp64 on exactly widened bf16 inputs.
+ */
+typedef struct {
+    const uint16_t *q, *k, *v, *dout;
+    int B, H, Hkv, S, D, causal;
+    double scale;
+    double *dq, *dk, *dv;       /* full mode: [B,S,H,D], [B,S,Hkv,D] x2 */
+    const int64_t *rows;        /* dq-rows mode: flat ids (b*H + h)*S + s */
+    int64_t begin, end;         /* range of (b,g) groups or of rows */
+    int mode;                   /* 0: full gradients per (b,g), 1: dq rows */
+} bjob_t;
+
+/* one query row: dq row, and (when dk/dv are given) its share of dk, dv */
+static void bwd_row(const bjob_t *J, int b, int h, int s, double *x, double *dqr,
+                    double *dk, double *dv)
+{
+    const int D = J->D, g = h / (J->H / J->Hkv);
+    const int n_allowed = J->causal ? s + 1 : J->S;
+    const uint16_t *qr = J->q + (((int64_t)b * J->S + s) * J->H + h) * D;
+    const uint16_t *dor = J->dout + (((int64_t)b * J->S + s) * J->H + h) * D;
+
+    double M = -INFINITY;
+    for (int t = 0; t < n_allowed; ++t) {
+        const uint16_t *kr = J->k + (((int64_t)b * J->S + t) * J->Hkv + g) * D;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc += widen_bf16(qr[d]) * widen_bf16(kr[d]);
+        x[t] = J->scale * acc;
+        if (x[t] > M)
+            M = x[t];
+    }
+    double L = 0.0;
+    for (int t = 0; t < n_allowed; ++t)
+        L += exp(x[t] - M);
+
+    /* x[t] becomes p_t; dp kept in x[S + t] */
+    double *dp = x + J->S;
+    double delta = 0.0;
+    for (int t = 0; t < n_allowed; ++t) {
+        x[t] = exp(x[t] - M) / L;
+        const uint16_t *vr = J->v + (((int64_t)b * J->S + t) * J->Hkv + g) * D;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc += widen_bf16(dor[d]) * widen_bf16(vr[d]);
+        dp[t] = acc;
+        delta += x[t] * acc;
+    }
+    for (int d = 0; d < D; ++d)
+        dqr[d] = 0.0;
+    for (int t = 0; t < n_allowed; ++t) {
+        const double ds = x[t] * (dp[t] - delta);
+        const int64_t kv = (((int64_t)b * J->S + t) * J->Hkv + g) * D;
+        const uint16_t *kr = J->k + kv;
+        for (int d = 0; d < D; ++d)
+            dqr[d] += J->scale * ds * widen_bf16(kr[d]);
+        if (dk) {
+            for (int d = 0; d < D; ++d) {
+                dk[kv + d] += J->scale * ds * widen_bf16(qr[d]);
+                dv[kv + d] += x[t] * widen_bf16(dor[d]);
+            }
+        }
+    }
+}
+
+static void *bwd_worker(void *arg)
+{
+    bjob_t *J = (bjob_t *)arg;
+    double *x = (double *)malloc(sizeof(double) * 2 * (size_t)J->S);
+    if (!x)
+        return (void *)1;
+    const int G = J->H / J->Hkv;
+    for (int64_t w = J->begin; w < J->end; ++w) {
+        if (J->mode == 0) {
+            /* group (b, g): every row of its query heads; this worker owns
+               dk/dv of the group, so the accumulation needs no lock */
+            const int b = (int)(w / J->Hkv), g = (int)(w % J->Hkv);
+            for (int hh = 0; hh < G; ++hh)
+                for (int s = 0; s < J->S; ++s) {
+                    const int h = g * G + hh;
+                    double *dqr = J->dq + (((int64_t)b * J->S + s) * J->H + h) * J->D;
+                    bwd_row(J, b, h, s, x, dqr, J->dk, J->dv);
+                }
+        } else {
+            int64_t id = J->rows[w];
+            const int s = (int)(id % J->S);
+            id /= J->S;
+            const int h = (int)(id % J->H), b = (int)(id / J->H);
+            bwd_row(J, b, h, s, x, J->dq + w * J->D, NULL, NULL);
+        }
+    }
+    free(x);
+    return NULL;
+}
+
+static int bwd_run(const bjob_t *base, int64_t n_units, int n_threads)
+{
+    if (n_threads <= 0)
+        n_threads = ora_default_threads();
+    if (n_threads > n_units)
+        n_threads = n_units > 0 ? (int)n_units : 1;
+    bjob_t *jobs = (bjob_t *)calloc((size_t)n_threads, sizeof(bjob_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return -2;
+    }
+    int rc = 0, started = 0;
+    for (int w = 0; w < n_threads; ++w) {
+        jobs[w] = *base;
+        jobs[w].begin = n_units * w / n_threads;
+        jobs[w].end = n_units * (w + 1) / n_threads;
+        if (pthread_create(&th[w], NULL, bwd_worker, &jobs[w]) != 0) {
+            rc = -2;
+            break;
+        }
+        ++started;
+    }
+    for (int w = 0; w < started; ++w) {
+        void *ret = NULL;
+        pthread_join(th[w], &ret);
+        if (ret)
+            rc = -2;
+    }
+    free(jobs);
+    free(th);
+    return rc;
+}
+
+/* Full gradients: dq [B,S,H,D], dk and dv [B,S,Hkv,D] (overwritten). */
+int ora_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                 int B, int H, int Hkv, int S, int D, int causal, double scale,
+                 double *dq, double *dk, double *dv, int n_threads)
+{
+    if (check_args(B, H, Hkv, S, D, 1))
+        return -1;
+    const size_t nkv = (size_t)B * S * Hkv * D;
+    memset(dk, 0, nkv * sizeof(double));
+    memset(dv, 0, nkv * sizeof(double));
+    bjob_t J = {q, k, v, dout, B, H, Hkv, S, D, causal, scale, dq, dk, dv, NULL, 0, 0, 0};
+    return bwd_run(&J, (int64_t)B * Hkv, n_threads);
+}
+
+/* dq of selected query rows only: dq [n_rows, D] for flat ids (b*H + h)*S + s. */
+int ora_attn_bwd_dq(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                    int B, int H, int Hkv, int S, int D, int causal, double scale,
+                    const int64_t *rows, int64_t n_rows, double *dq, int n_threads)
+{
+    if (check_args(B, H, Hkv, S, D, 1) || !rows || n_rows <= 0)
+        return -1;
+    bjob_t J = {q, k, v, dout, B, H, Hkv, S, D, causal, scale, dq, NULL, NULL, rows, 0, 0, 1};
+    return bwd_run(&J, n_rows, n_threads);
 }

@@ -1,5 +1,6 @@
 """Plant plausible mistakes in the oracle (on the CPU) and check that the pins
-in ``test_oracle_pins.py`` catch every one of them.
+in ``test_oracle_pins.py`` and ``test_oracle_bwd_pins.py`` catch every one of
+them.
 
 Each mutant is ``oracle/ora.c`` with one textual change, compiled into a
 temporary library and loaded by a child pytest run through ``RA_ORACLE_LIB``.
@@ -35,6 +36,21 @@ MUTANTS = {
                                     "                if (!any) {\n                    o[0] = 1.0;\n                    *l = -INFINITY;")],
     "ring_skips_last_chunk": [("for (int step = 0; step < J->P; ++step)",
                                "for (int step = 0; step < J->P - (J->P > 1); ++step)")],
+    # backward pass
+    "bwd_drops_delta": [("const double ds = x[t] * (dp[t] - delta);",
+                         "const double ds = x[t] * dp[t];")],
+    "bwd_dk_unscaled": [("dk[kv + d] += J->scale * ds * widen_bf16(qr[d]);",
+                         "dk[kv + d] += ds * widen_bf16(qr[d]);")],
+    "bwd_dv_uses_ds": [("dv[kv + d] += x[t] * widen_bf16(dor[d]);",
+                        "dv[kv + d] += ds * widen_bf16(dor[d]);")],
+    "bwd_dp_uses_query": [("acc += widen_bf16(dor[d]) * widen_bf16(vr[d]);",
+                           "acc += widen_bf16(dor[d]) * widen_bf16(qr[d]);")],
+    "bwd_dq_uses_value_rows": [("const uint16_t *kr = J->k + kv;", "const uint16_t *kr = J->v + kv;")],
+    "bwd_group_mapping": [("const int D = J->D, g = h / (J->H / J->Hkv);",
+                           "const int D = J->D, g = h % J->Hkv;")],
+    "bwd_causal_excludes_diagonal": [("    const int n_allowed = J->causal ? s + 1 : J->S;",
+                                      "    const int n_allowed = J->causal ? (s > 0 ? s : 1) : J->S;")],
+    "bwd_delta_unweighted": [("delta += x[t] * acc;", "delta += acc;")],
 }
 
 
@@ -43,7 +59,8 @@ def _child(env_lib):
     if env_lib:
         env["RA_ORACLE_LIB"] = env_lib
     return subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                           os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                           os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                           os.path.join(ROOT, "tests", "test_oracle_bwd_pins.py")],
                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
 
 
