@@ -69,11 +69,11 @@ def _load():
         lib.ora_attn_block.restype = i
         lib.ora_merge.argtypes = [f64p, f64p, i, i, i, i, i, f64p, f64p]
         lib.ora_merge.restype = i
-        lib.ora_attn_bwd.argtypes = [u16p, u16p, u16p, u16p, i, i, i, i, i, i, ctypes.c_double,
-                                     f64p, f64p, f64p, i]
+        lib.ora_attn_bwd.argtypes = [u16p, u16p, u16p, u16p, u16p, i, i, i, i, i, i,
+                                     ctypes.c_double, f64p, f64p, f64p, i]
         lib.ora_attn_bwd.restype = i
-        lib.ora_attn_bwd_dq.argtypes = [u16p, u16p, u16p, u16p, i, i, i, i, i, i, ctypes.c_double,
-                                        i64p, ctypes.c_int64, f64p, i]
+        lib.ora_attn_bwd_dq.argtypes = [u16p, u16p, u16p, u16p, u16p, i, i, i, i, i, i,
+                                        ctypes.c_double, i64p, ctypes.c_int64, f64p, i]
         lib.ora_attn_bwd_dq.restype = i
         lib.ora_default_threads.argtypes = []
         lib.ora_default_threads.restype = i
@@ -192,19 +192,23 @@ def merge(o_parts: np.ndarray, lse_parts: np.ndarray):
     return out, lse
 
 
-def attn_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0):
+def attn_bwd(q, k, v, dout, causal: bool, scale: float, out=None, threads: int = 0):
     """Gradients of ``sum(out * dout)`` for the attention above (the
-    derivative of the definition; see ``ora.c``).  Returns fp64 ``dq``
-    [B,S,H,D], ``dk`` and ``dv`` [B,S,Hkv,D]."""
+    derivative of the definition; see ``ora.c``).  ``out``: optional bf16
+    forward output [B,S,H,D] that delta = <dout, out> is taken from (exact
+    delta when None).  Returns fp64 ``dq`` [B,S,H,D], ``dk`` and ``dv``
+    [B,S,Hkv,D]."""
     B, S, H, Hkv, D = _shapes(q, k, v)
     assert tuple(dout.shape) == tuple(q.shape)
     qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+    ob = None if out is None else _bits(out)
+    assert ob is None or ob.shape == tuple(q.shape)
     dq = np.empty((B, S, H, D), np.float64)
     dk = np.empty((B, S, Hkv, D), np.float64)
     dv = np.empty((B, S, Hkv, D), np.float64)
     rc = _load().ora_attn_bwd(
         _ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16), _ptr(vb, ctypes.c_uint16),
-        _ptr(db, ctypes.c_uint16), B, H, Hkv, S, D, int(bool(causal)), float(scale),
+        _ptr(db, ctypes.c_uint16), None if ob is None else _ptr(ob, ctypes.c_uint16), B, H, Hkv, S, D, int(bool(causal)), float(scale),
         _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
         int(threads))
     if rc != 0:
@@ -212,16 +216,21 @@ def attn_bwd(q, k, v, dout, causal: bool, scale: float, threads: int = 0):
     return dq, dk, dv
 
 
-def attn_bwd_dq(q, k, v, dout, causal: bool, scale: float, rows, threads: int = 0):
-    """``dq`` of selected query rows (flat ids ``(b*H + h)*S + s``), [n, D]."""
+def attn_bwd_dq(q, k, v, dout, causal: bool, scale: float, rows, out_rows=None,
+                threads: int = 0):
+    """``dq`` of selected query rows (flat ids ``(b*H + h)*S + s``), [n, D].
+    ``out_rows``: optional bf16 forward output of those rows [n, D] that
+    delta is taken from (exact delta when None)."""
     B, S, H, Hkv, D = _shapes(q, k, v)
     qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
     rows_a = np.ascontiguousarray(rows, dtype=np.int64)
+    ob = None if out_rows is None else _bits(out_rows)
+    assert ob is None or ob.shape == (len(rows_a), D)
     dq = np.empty((len(rows_a), D), np.float64)
     rc = _load().ora_attn_bwd_dq(
         _ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16), _ptr(vb, ctypes.c_uint16),
-        _ptr(db, ctypes.c_uint16), B, H, Hkv, S, D, int(bool(causal)), float(scale),
-        _ptr(rows_a, ctypes.c_int64), len(rows_a), _ptr(dq, ctypes.c_double), int(threads))
+        _ptr(db, ctypes.c_uint16), None if ob is None else _ptr(ob, ctypes.c_uint16), B, H, Hkv, S,
+        D, int(bool(causal)), float(scale), _ptr(rows_a, ctypes.c_int64), len(rows_a), _ptr(dq, ctypes.c_double), int(threads))
     if rc != 0:
         raise ValueError(f"ora_attn_bwd_dq failed ({rc})")
     return dq

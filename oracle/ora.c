@@ -412,9 +412,16 @@ int ora_merge(const double *o_parts, const double *lse_parts, int n,
  *   dv[b,t,g,:] += p_t dout[b,s,h,:]               the query heads of group g)
  *
  * Every step in fp64 on exactly widened bf16 inputs.
+ *
+ * delta can also be taken from a given forward output: when `out` (bf16,
+ * [B,S,H,D], or one row per sampled query in the dq-rows mode) is passed,
+ * delta = <dout[b,s,h,:], out[b,s,h,:]> on that output, which is how a
+ * backward pass that receives the forward's stored (rounded) output defines
+ * it.  With out == NULL delta is the exact sum above.
  */
 typedef struct {
     const uint16_t *q, *k, *v, *dout;
+    const uint16_t *out;        /* optional: [B,S,H,D] (full) or [n_rows,D] (dq rows) */
     int B, H, Hkv, S, D, causal;
     double scale;
     double *dq, *dk, *dv;       /* full mode: [B,S,H,D], [B,S,Hkv,D] x2 */
@@ -424,8 +431,8 @@ typedef struct {
 } bjob_t;
 
 /* one query row: dq row, and (when dk/dv are given) its share of dk, dv */
-static void bwd_row(const bjob_t *J, int b, int h, int s, double *x, double *dqr,
-                    double *dk, double *dv)
+static void bwd_row(const bjob_t *J, int b, int h, int s, const uint16_t *outr, double *x,
+                    double *dqr, double *dk, double *dv)
 {
     const int D = J->D, g = h / (J->H / J->Hkv);
     const int n_allowed = J->causal ? s + 1 : J->S;
@@ -457,6 +464,11 @@ static void bwd_row(const bjob_t *J, int b, int h, int s, double *x, double *dqr
             acc += widen_bf16(dor[d]) * widen_bf16(vr[d]);
         dp[t] = acc;
         delta += x[t] * acc;
+    }
+    if (outr) {  /* delta from the given forward output row instead */
+        delta = 0.0;
+        for (int d = 0; d < D; ++d)
+            delta += widen_bf16(dor[d]) * widen_bf16(outr[d]);
     }
     for (int d = 0; d < D; ++d)
         dqr[d] = 0.0;
@@ -490,15 +502,16 @@ static void *bwd_worker(void *arg)
             for (int hh = 0; hh < G; ++hh)
                 for (int s = 0; s < J->S; ++s) {
                     const int h = g * G + hh;
-                    double *dqr = J->dq + (((int64_t)b * J->S + s) * J->H + h) * J->D;
-                    bwd_row(J, b, h, s, x, dqr, J->dk, J->dv);
+                    const int64_t ri = (((int64_t)b * J->S + s) * J->H + h) * J->D;
+                    bwd_row(J, b, h, s, J->out ? J->out + ri : NULL, x, J->dq + ri, J->dk, J->dv);
                 }
         } else {
             int64_t id = J->rows[w];
             const int s = (int)(id % J->S);
             id /= J->S;
             const int h = (int)(id % J->H), b = (int)(id / J->H);
-            bwd_row(J, b, h, s, x, J->dq + w * J->D, NULL, NULL);
+            bwd_row(J, b, h, s, J->out ? J->out + w * J->D : NULL, x, J->dq + w * J->D, NULL,
+                    NULL);
         }
     }
     free(x);
@@ -540,27 +553,30 @@ static int bwd_run(const bjob_t *base, int64_t n_units, int n_threads)
     return rc;
 }
 
-/* Full gradients: dq [B,S,H,D], dk and dv [B,S,Hkv,D] (overwritten). */
+/* Full gradients: dq [B,S,H,D], dk and dv [B,S,Hkv,D] (overwritten); out may
+   be NULL (exact delta) or the forward output [B,S,H,D] that delta is taken from. */
 int ora_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
-                 int B, int H, int Hkv, int S, int D, int causal, double scale,
-                 double *dq, double *dk, double *dv, int n_threads)
+                 const uint16_t *out, int B, int H, int Hkv, int S, int D, int causal,
+                 double scale, double *dq, double *dk, double *dv, int n_threads)
 {
     if (check_args(B, H, Hkv, S, D, 1))
         return -1;
     const size_t nkv = (size_t)B * S * Hkv * D;
     memset(dk, 0, nkv * sizeof(double));
     memset(dv, 0, nkv * sizeof(double));
-    bjob_t J = {q, k, v, dout, B, H, Hkv, S, D, causal, scale, dq, dk, dv, NULL, 0, 0, 0};
+    bjob_t J = {q, k, v, dout, out, B, H, Hkv, S, D, causal, scale, dq, dk, dv, NULL, 0, 0, 0};
     return bwd_run(&J, (int64_t)B * Hkv, n_threads);
 }
 
-/* dq of selected query rows only: dq [n_rows, D] for flat ids (b*H + h)*S + s. */
+/* dq of selected query rows only: dq [n_rows, D] for flat ids (b*H + h)*S + s;
+   out_rows may be NULL (exact delta) or the forward output rows [n_rows, D]. */
 int ora_attn_bwd_dq(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
-                    int B, int H, int Hkv, int S, int D, int causal, double scale,
-                    const int64_t *rows, int64_t n_rows, double *dq, int n_threads)
+                    const uint16_t *out_rows, int B, int H, int Hkv, int S, int D, int causal,
+                    double scale, const int64_t *rows, int64_t n_rows, double *dq, int n_threads)
 {
     if (check_args(B, H, Hkv, S, D, 1) || !rows || n_rows <= 0)
         return -1;
-    bjob_t J = {q, k, v, dout, B, H, Hkv, S, D, causal, scale, dq, NULL, NULL, rows, 0, 0, 1};
+    bjob_t J = {q, k, v, dout, out_rows, B, H, Hkv, S, D, causal, scale, dq, NULL, NULL,
+                rows, 0, 0, 1};
     return bwd_run(&J, n_rows, n_threads);
 }

@@ -14,7 +14,9 @@ the attention definition.  What fixes that derivative independently:
   sum_t dk_t = 0 for every (b, KV head); the weights of a row sum to one, so
   sum_t dv_t = sum of dout over the group's rows;
 * GQA equals MHA on repeated K/V with dk/dv summed over the group;
-* the row-sampled dq equals the full dq.
+* the row-sampled dq equals the full dq;
+* taking delta from a given rounded output shifts dq and dk by closed forms
+  in the shift of delta and leaves dv bit-identical.
 """
 import numpy as np
 import pytest
@@ -152,3 +154,33 @@ def test_bwd_rejects_bad_shapes(oracle_mod):
     k = torch.zeros(1, 16, 2, 8).bfloat16()
     with pytest.raises(ValueError):
         oracle_mod.attn_bwd(q, k, k, q, True, 0.1)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_delta_from_given_output_shifts_by_closed_form(oracle_mod, causal):
+    """With delta taken from a given (rounded) output instead of exactly,
+    ds_st changes by -p_st * d_s where d_s = <dout_s, out_given_s - out_s>;
+    hence dq_s moves by -scale * d_s * sum_t p_st k_t, dk_t by
+    -scale * sum_s p_st d_s q_s, and dv does not move at all."""
+    w = Workload("od", 1, 4, 2, 64, 16, 1, causal, sigma_qk=2.0)
+    q, k, v = make_inputs(w, seed=15)
+    do = _dout(q.shape, 16)
+    out, _, p = oracle_mod.attn_direct(q, k, v, causal, w.scale, return_weights=True)
+    out_b = torch.tensor(out).bfloat16()
+    e = oracle_mod.attn_bwd(q, k, v, do, causal, w.scale)
+    g = oracle_mod.attn_bwd(q, k, v, do, causal, w.scale, out=out_b)
+    assert np.array_equal(g[2], e[2])
+    B, S, H, D, G = w.B, w.S, w.H, w.D, w.H // w.Hkv
+    d = np.einsum("bshd,bshd->bhs", _np(do), _np(out_b) - out)        # [B,H,S]
+    pw = p.reshape(B, H, S, S)                                          # p[b,h,s,t]
+    kk, qq = np.repeat(_np(k), G, axis=2), _np(q)
+    ddq = -w.scale * np.einsum("bhs,bhst,bthd->bshd", d, pw, kk)
+    ddk = -w.scale * np.einsum("bhs,bhst,bshd->bthd", d, pw, qq).reshape(B, S, w.Hkv, G, D).sum(3)
+    assert np.abs(d).max() > 1e-4  # the rounding does move delta
+    np.testing.assert_allclose(g[0] - e[0], ddq, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(g[1] - e[1], ddk, atol=1e-12, rtol=0)
+    # the dq-rows mode takes the same rows of the given output
+    rows = np.array([0, 5, 63, 2 * 64 + 9], dtype=np.int64)
+    s_, h_ = rows % S, (rows // S) % H
+    got = oracle_mod.attn_bwd_dq(q, k, v, do, causal, w.scale, rows, out_rows=out_b[0, s_, h_])
+    assert np.array_equal(got, g[0][0, s_, h_])

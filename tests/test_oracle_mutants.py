@@ -51,6 +51,8 @@ MUTANTS = {
     "bwd_causal_excludes_diagonal": [("    const int n_allowed = J->causal ? s + 1 : J->S;",
                                       "    const int n_allowed = J->causal ? (s > 0 ? s : 1) : J->S;")],
     "bwd_delta_unweighted": [("delta += x[t] * acc;", "delta += acc;")],
+    "bwd_given_output_row_misread": [("delta += widen_bf16(dor[d]) * widen_bf16(outr[d]);",
+                                      "delta += widen_bf16(dor[d]) * widen_bf16(outr[0]);")],
 }
 
 
