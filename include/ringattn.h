@@ -1,6 +1,6 @@
 /*
  * ringattn.h -- C ABI of libringattn: single-GPU ring-chunked attention
- * forward for NVIDIA GB300 (sm_103a).
+ * forward (and its backward pass) for NVIDIA GB300 (sm_103a).
  *
  * The method is the compute side of the "Ring Attention" fused kernel of the
  * mKernel overview page (chatgpz.de, German translation of the MarkTechPost
@@ -121,6 +121,48 @@ ra_status ra_merge_partials(const void* o_parts, int o_is_fp32, const float* lse
                             void* out, float* lse, int B, int H, int S, int D, void* stream);
 
 /*
+ * ra_bwd_workspace_bytes -- bytes of device workspace ra_bwd needs: two fp32
+ * values per query row (8 * B * H * S).  Returns 0 if a size is not positive.
+ */
+unsigned long long ra_bwd_workspace_bytes(int B, int H, int S);
+
+/*
+ * ra_bwd -- gradients of ra_fwd's output with respect to q, k and v, for a
+ * given gradient dout of the output (the loss sum(out * dout)).  The pages
+ * describe no backward pass; this is the derivative of the definition in
+ * ra_fwd's comment, with p_st = softmax_t(x) of query row s:
+ *     dp_st   = <dout[b,s,h,:], v[b,t,g,:]>
+ *     delta_s = <dout[b,s,h,:], out[b,s,h,:]>   (= sum_t p_st dp_st)
+ *     ds_st   = p_st (dp_st - delta_s)
+ *     dq[b,s,h,:] = scale * sum_t ds_st k[b,t,g,:]
+ *     dk[b,t,g,:] = scale * sum over rows s and query heads h of group g of ds_st q[b,s,h,:]
+ *     dv[b,t,g,:] =         sum over rows s and query heads h of group g of p_st dout[b,s,h,:]
+ * p_st is recomputed from q, k and lse; the key tiles of each query tile are
+ * visited in ra_fwd's ring order for P (only the rounding order depends on P).
+ *
+ *   q, out, dout [B, S, H, D] bf16, contiguous; out and lse as ra_fwd wrote
+ *                them for the same q, k, v, P, causal and scale
+ *   k, v         [B, S, Hkv, D] bf16, contiguous
+ *   lse          [B, H, S] fp32 (natural log), 4-byte aligned
+ *   dq           [B, S, H, D] bf16, written
+ *   dk, dv       [B, S, Hkv, D] bf16, written
+ *   workspace    device memory of workspace_bytes >= ra_bwd_workspace_bytes(B, H, S)
+ *                bytes, owned by the caller, 16-byte aligned; overwritten (no
+ *                initial contents needed); a workspace must not be shared by
+ *                two ra_bwd calls that can run at the same time
+ *   Same shape, support and stream rules as ra_fwd; every bf16 pointer 16-byte
+ *   aligned; dq, dk, dv must not overlap each other or any input.
+ * Enqueues three kernels on `stream` (per-row sums, dk/dv, dq).  Every output
+ * element is written exactly once, so the result does not depend on timing.
+ * Errors as ra_fwd; RA_ERR_INVALID_ARG also for a null lse or workspace and for
+ * a workspace smaller than ra_bwd_workspace_bytes(B, H, S).
+ */
+ra_status ra_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                 unsigned long long workspace_bytes, int B, int H, int Hkv, int S, int D, int P,
+                 int causal, float scale, void* stream);
+
+/*
  * ra_get_last_device_status -- synchronise `stream`, then read and clear this
  * device's sticky status word.  Returns RA_ERR_TIMEOUT if any kernel launched
  * since the previous query gave up a bounded wait (its outputs are then not
@@ -139,7 +181,7 @@ int ra_version(void);
 
 /*
  * Test hook for the failure path: when `timeout_ns` > 0, subsequent ra_fwd
- * launches on this process use that wait limit instead of the default (2 s);
+ * and ra_bwd launches on this process use that wait limit instead of the default (2 s);
  * when `skip_value_load` != 0 the producer deliberately never issues the
  * first value-tile copy, so the consumer's bounded wait must run out and the
  * launch must report RA_ERR_TIMEOUT.  Pass (0, 0) to restore normal launches.

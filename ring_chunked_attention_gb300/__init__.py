@@ -9,6 +9,8 @@ cannot be loaded, every call raises.
 Functions carry the C names:
 
 * :func:`ra_fwd` -- ring-chunked attention forward (out, lse);
+* :func:`ra_fwd_block` -- one ring step (a query block against a key/value block);
+* :func:`ra_bwd` -- gradients dq, dk, dv of the forward for a given dout;
 * :func:`ra_merge_partials` -- merge normalised partials over disjoint key sets;
 * :func:`ra_get_last_device_status`, :func:`ra_status_string`,
   :func:`ra_debug_set_fault`, :func:`ra_shutdown`.
@@ -18,7 +20,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["ra_fwd", "ra_fwd_block", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+__all__ = ["ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
            "ra_debug_set_fault", "ra_set_mma_order", "ra_shutdown", "ra_version", "RaError", "library_path",
            "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT"]
 
@@ -28,7 +30,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libringattn.so")
 _lib = None
 
-EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
            "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_set_mma_order",
            "ra_shutdown")
 
@@ -58,6 +60,11 @@ def _load():
     ll = ctypes.c_longlong
     lib.ra_fwd_block.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ll, ll, i, f, vp]
     lib.ra_fwd_block.restype = i
+    ull = ctypes.c_ulonglong
+    lib.ra_bwd_workspace_bytes.argtypes = [i, i, i]
+    lib.ra_bwd_workspace_bytes.restype = ull
+    lib.ra_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ull, i, i, i, i, i, i, i, f, vp]
+    lib.ra_bwd.restype = i
     lib.ra_merge_partials.argtypes = [vp, i, vp, i, vp, vp, i, i, i, i, vp]
     lib.ra_merge_partials.restype = i
     lib.ra_get_last_device_status.argtypes = [vp]
@@ -162,6 +169,50 @@ def ra_fwd_block(q, k, v, *, q_pos0: int, k_pos0: int, causal: bool, scale: floa
                             _stream_ptr(stream))
     _check(code, "ra_fwd_block")
     return out, lse
+
+
+def ra_bwd_workspace_bytes(B: int, H: int, S: int) -> int:
+    """Device workspace bytes :func:`ra_bwd` needs (8 * B * H * S)."""
+    return int(_load().ra_bwd_workspace_bytes(int(B), int(H), int(S)))
+
+
+def ra_bwd(q, k, v, out, lse, dout, *, P: int, causal: bool, scale: float | None = None,
+           dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of :func:`ra_fwd` for output gradient ``dout`` [B,S,H,D] bf16.
+    ``out`` and ``lse`` are the forward's results for the same inputs and
+    options.  Returns ``(dq, dk, dv)`` (bf16, shapes of q, k, v); buffers and
+    the workspace are allocated with torch when not given."""
+    import torch
+
+    lib = _load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{n} must be a contiguous 4-D bf16 CUDA tensor")
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != (B, S, Hkv, D):
+        raise ValueError("k and v must be [B,S,Hkv,D] matching q")
+    if tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("out and dout must have q's shape")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [B,H,S] fp32 tensor")
+    if scale is None:
+        scale = D ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, ref, n in ((dq, q, "dq"), (dk, k, "dk"), (dv, v, "dv")):
+        if t.dtype != torch.bfloat16 or tuple(t.shape) != tuple(ref.shape) or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous bf16 tensor shaped like its input")
+    need = ra_bwd_workspace_bytes(B, H, S)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    code = lib.ra_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                      workspace.data_ptr(), workspace.numel() * workspace.element_size(), B, H, Hkv,
+                      S, D, int(P), int(bool(causal)), float(scale), _stream_ptr(stream))
+    _check(code, "ra_bwd")
+    return dq, dk, dv
 
 
 def ra_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_ptr: int | None, B: int,

@@ -141,10 +141,6 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-extern "C" {
-
-}  // extern "C"
-
 namespace {
 
 // Shared tail of ra_fwd and ra_fwd_block: device check, tensor maps, work
@@ -276,6 +272,81 @@ ra_status ra_merge_partials(const void* o_parts, int o_is_fp32, const float* lse
   return RA_OK;
 }
 
+unsigned long long ra_bwd_workspace_bytes(int B, int H, int S) {
+  if (B <= 0 || H <= 0 || S <= 0) return 0;
+  return (unsigned long long)B * (unsigned long long)H * (unsigned long long)S * 8ull;
+}
+
+ra_status ra_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                 unsigned long long workspace_bytes, int B, int H, int Hkv, int S, int D, int P,
+                 int causal, float scale, void* stream) {
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return RA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || P <= 0) return RA_ERR_INVALID_ARG;
+  if (H % Hkv != 0 || S % P != 0) return RA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return RA_ERR_INVALID_ARG;
+  if (workspace_bytes < ra_bwd_workspace_bytes(B, H, S)) return RA_ERR_INVALID_ARG;
+  if (scale < 0.0f) return RA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
+  if ((S / P) % 128 != 0) return RA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return RA_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return RA_ERR_UNSUPPORTED;
+  if ((long long)B * S >= (1ll << 31) || (long long)B * H * (S / 128) >= (1ll << 31))
+    return RA_ERR_UNSUPPORTED;
+
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  if (!dev->sm103) return RA_ERR_UNSUPPORTED;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = tensor_map(q, (long long)B * S, H, D, &tq)) != RA_OK) return st;
+  if ((st = tensor_map(k, (long long)B * S, Hkv, D, &tk)) != RA_OK) return st;
+  if ((st = tensor_map(v, (long long)B * S, Hkv, D, &tv)) != RA_OK) return st;
+  if ((st = tensor_map(dout, (long long)B * S, H, D, &tdo)) != RA_OK) return st;
+
+  ra::BwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.out = out;
+  a.dout = dout;
+  a.lse = lse;
+  a.nlse2 = static_cast<float*>(workspace);
+  a.ndelta = a.nlse2 + (size_t)B * H * S;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.status = dev->status;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.S = S;
+  a.P = P;
+  a.causal = causal ? 1 : 0;
+  a.tiles = S / 128;
+  a.tpc = S / P / 128;
+  a.scale = scale;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    a.timeout_ns = g_timeout_ns;
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long units = (long long)B * S * H * (D / 8);
+  long long grid = (units + 255) / 256;
+  if (grid > (long long)dev->sms * 8) grid = (long long)dev->sms * 8;
+  cudaError_t e = ra::launch_bwd_prep(D, a, (int)grid, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  a.n_items = B * Hkv * a.tiles;
+  e = ra::launch_bwd_dkdv(D, tq, tk, tv, tdo, a, a.n_items < dev->sms ? a.n_items : dev->sms, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  a.n_items = B * H * a.tiles;
+  e = ra::launch_bwd_dq(D, tq, tk, tv, tdo, a, a.n_items < dev->sms ? a.n_items : dev->sms, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return RA_OK;
+}
+
 ra_status ra_get_last_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -298,7 +369,7 @@ const char* ra_status_string(ra_status s) {
 
 int ra_last_cuda_error(void) { return g_last_cuda_error; }
 
-int ra_version(void) { return (0 << 16) | (1 << 8) | 0; }
+int ra_version(void) { return (0 << 16) | (2 << 8) | 0; }
 
 void ra_debug_set_fault(long long timeout_ns, int skip_value_load) {
   std::lock_guard<std::mutex> lock(g_mu);

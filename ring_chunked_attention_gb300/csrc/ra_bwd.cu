@@ -1,0 +1,891 @@
+// ra_bwd.cu -- backward pass of the ring-chunked attention: dq, dk, dv for a
+// given output gradient, on sm_103a tensor cores (tcgen05, tensor memory, TMA).
+//
+// The pages describe no backward pass.  What is computed is the gradient of
+// the forward's definition (exact softmax attention), for one query row s of
+// head h and a key t of its KV head g:
+//   p_st    = exp(scale * q_s.k_t - lse_s)       (lse from the forward)
+//   dp_st   = dout_s . v_t
+//   delta_s = sum_d out_s[d] dout_s[d]            (= sum_t p_st dp_st)
+//   ds_st   = p_st (dp_st - delta_s)
+//   dq_s = scale sum_t ds_st k_t,  dk_t = scale sum_s ds_st q_s,  dv_t = sum_s p_st dout_s
+// with dk, dv summed over the query heads of the GQA group.
+//
+// Three kernels, launched in order on one stream:
+//   bwd_prep_kernel  -delta_s and -lse_s*log2(e) per query row (row sums,
+//                    HBM-bound) into the caller's workspace;
+//   bwd_dkdv_kernel  one 128-key tile of one KV head per work item: the K/V
+//                    tiles stay in shared memory while the q/dout tiles of
+//                    every query head of the group stream past; dk and dv
+//                    accumulate in tensor memory;
+//   bwd_dq_kernel    one 128-row query tile per work item: q/dout stay in
+//                    shared memory while the K/V tiles stream past in the
+//                    forward's ring order (own chunk first); dq accumulates in
+//                    tensor memory.
+// Every output element is written once (no atomics), so results are
+// deterministic.  Splitting dq from dk/dv recomputes S and dP in both
+// tensor-core kernels (7 tile MMAs per query/key tile pair instead of 5) in
+// exchange for no fp32 dq scratch and no atomic traffic.
+//
+// CTA organisation of both tensor-core kernels (one persistent CTA per SM):
+//   warps 0-3  elementwise work, one thread per TMEM lane (query row in the
+//              dq kernel, key row in the dk/dv kernel), and the epilogue
+//   warp  4    TMA producer
+//   warp  5    MMA issuer (one thread)
+// Every wait is bounded as in the forward kernel: on timeout the CTA sets the
+// status word, drains its copies and MMAs, frees tensor memory and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ra_internal.h"
+#include "ra_ptx.cuh"
+#include "ra_umma.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdWarpTma = 4;
+constexpr int kBwdWarpMma = 5;
+constexpr int kT = 128;                // rows per tile (queries or keys)
+constexpr int kBlk = 128 * 128;        // one [128 rows x 64 cols] bf16 block
+constexpr uint32_t kBwdTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------ MMAs
+// D[128 x 128] = A[128 x DH] * B[128 x DH]^T, A and B K-major tiles.
+template <int DH>
+__device__ __forceinline__ void mma_nt(uint32_t tD, uint32_t a_lo, uint32_t b_lo) {
+  constexpr uint32_t idesc = make_idesc(kT, kT, 0);
+#pragma unroll
+  for (int kk = 0; kk < DH / 16; ++kk) {
+    const uint32_t off = (uint32_t)((kk >> 2) * kBlk + (kk & 3) * 32) >> 4;
+    mma_ss_lh(tD, a_lo + off, kDescHiSw128, b_lo + off, kDescHiSw128, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[128 x DH] (+)= A[128 x 128] (bf16 pairs in tensor memory) * B[128 x DH]
+// (an MN-major tile in shared memory).
+template <int DH>
+__device__ __forceinline__ void mma_tn(uint32_t tD, uint32_t tA, uint32_t b_lo, bool accumulate) {
+  constexpr uint32_t idesc = make_idesc(kT, DH, 1);
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk)
+    mma_ts_lh(tD, tA + kk * 8, b_lo + (uint32_t)(kk * (2048 >> 4)), kDescHiSw128, idesc,
+              (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// ------------------------------------------------------------- waits
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      const BwdArgs& a) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, a.timeout_ns, a.status);
+}
+
+__device__ __forceinline__ bool bwait_warp(uint32_t bar, uint32_t parity,
+                                           volatile int* abort_flag, const BwdArgs& a) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = bwait(bar, parity, abort_flag, a) ? 1 : 0;
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// all four warps of the elementwise warpgroup arrive once each
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// k-th work item of this CTA: snake order over rounds of gridDim.x items
+__device__ __forceinline__ int bwd_item_index(int k) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+// ------------------------------------------------------- elementwise pieces
+// p = exp2(x * scale*log2e - lse*log2e) for 32 scores of one row, in place
+// (fp32 bit patterns).  kMask: zero every column c with c > lim (dq kernel,
+// keys past the query row) or c < lim (dk/dv kernel, queries before the key
+// row), selected by kKeyRows.  nl2 points at per-column values (dk/dv kernel)
+// or is null with nl2x2 holding the row's value (dq kernel).
+template <bool kMask, bool kKeyRows>
+__device__ __forceinline__ void exp_chunk(uint32_t (&s)[32], int c0, int lim, uint64_t c2,
+                                          uint64_t nl2x2, const float* nl2) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    uint64_t bias = nl2x2;
+    if (nl2) bias = *reinterpret_cast<const uint64_t*>(nl2 + c0 + j);
+    const uint64_t xs = f2_fma(f2_pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), c2, bias);
+    float p0 = ex2(f2_lo(xs)), p1 = ex2(f2_hi(xs));
+    if (kMask) {
+      if (kKeyRows) {
+        p0 = (c0 + j < lim) ? 0.0f : p0;
+        p1 = (c0 + j + 1 < lim) ? 0.0f : p1;
+      } else {
+        p0 = (c0 + j > lim) ? 0.0f : p0;
+        p1 = (c0 + j + 1 > lim) ? 0.0f : p1;
+      }
+    }
+    s[j] = __float_as_uint(p0);
+    s[j + 1] = __float_as_uint(p1);
+  }
+}
+
+// 32 weights -> 16 packed bf16 pairs
+__device__ __forceinline__ void pack_chunk(const uint32_t (&p)[32], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1]));
+}
+
+// ds = p (dp - delta) for 32 columns -> 16 packed bf16 pairs.  ndl: -delta per
+// column (dk/dv kernel) or null with ndl2 holding the row's -delta (dq kernel);
+// the sum dp + (-delta) is the subtraction.
+__device__ __forceinline__ void ds_chunk(const uint32_t (&p)[32], const uint32_t (&dp)[32], int c0,
+                                         uint64_t ndl2, const float* ndl, uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    uint64_t nd = ndl2;
+    if (ndl) nd = *reinterpret_cast<const uint64_t*>(ndl + c0 + j);
+    const uint64_t d = f2_add(f2_pack(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])), nd);
+    const uint64_t ds = f2_mul(f2_pack(__uint_as_float(p[j]), __uint_as_float(p[j + 1])), d);
+    pk[j >> 1] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
+  }
+}
+
+// D fp32 accumulator columns of this thread's TMEM lane -> bf16 row in global
+// memory, times `mul`.
+template <int DH>
+__device__ __forceinline__ void store_row(uint32_t tAcc, float mul, __nv_bfloat16* dst) {
+  uint4* row = reinterpret_cast<uint4*>(dst);
+#pragma unroll 1
+  for (int c0 = 0; c0 < DH; c0 += 32) {
+    uint32_t o[32];
+    tmem_ld32(tAcc + c0, o);
+    tmem_wait_ld_regs(o);
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      row[c0 / 8 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  }
+}
+
+// ====================================================== row sums (prep)
+// -delta_s = -sum_d out[s,d] dout[s,d] and -lse_s*log2(e), per query row.  DH/8
+// threads per row, each reading 16 bytes of out and of dout.
+template <int DH>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
+  constexpr int per = DH / 8;
+  const long long rows = (long long)a.B * a.S * a.H;  // [B,S,H] order
+  const long long units = rows * per;
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long w0 = (long long)blockIdx.x * blockDim.x + (threadIdx.x - lane); w0 < units;
+       w0 += stride) {
+    const long long w = w0 + lane;
+    const bool active = w < units;
+    const long long row = w / per;
+    const int cpart = (int)(w - row * per);
+    float acc = 0.0f;
+    if (active) {
+      const long long e0 = row * DH + cpart * 8;
+      const uint4 o = __ldcs(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out) + e0));
+      const uint4 g = __ldcs(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + e0));
+      const uint32_t ov[4] = {o.x, o.y, o.z, o.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc = fmaf(__uint_as_float(ov[j] << 16), __uint_as_float(gv[j] << 16), acc);
+        acc = fmaf(__uint_as_float(ov[j] & 0xFFFF0000u), __uint_as_float(gv[j] & 0xFFFF0000u), acc);
+      }
+    }
+#pragma unroll
+    for (int o = per / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (active && cpart == 0) {
+      const int h = (int)(row % a.H);
+      const long long bs = row / a.H;
+      const int s = (int)(bs % a.S);
+      const long long b = bs / a.S;
+      const long long li = (b * a.H + h) * a.S + s;
+      a.ndelta[li] = -acc;
+      a.nlse2[li] = -a.lse[li] * kLog2e;
+    }
+  }
+}
+
+// ============================================================ dk / dv
+template <int DH>
+struct KvLayout {
+  static constexpr int DK = DH / 64;
+  static constexpr int NS = (DH == 128) ? 2 : 4;  // q/dout ring depth
+  static constexpr int TILE = kT * DH * 2;
+  static constexpr int K_OFF = 0, V_OFF = TILE;
+  static constexpr int STAGE = 2 * TILE + 1024;   // q, dout, -lse*log2e[128], -delta[128]
+  static constexpr int ST_OFF = 2 * TILE;
+  static constexpr int NL2_IN = 2 * TILE, DL_IN = 2 * TILE + 512;  // offsets inside a stage
+  static constexpr int BAR_OFF = ST_OFF + NS * STAGE;
+  static constexpr int KV_FULL = 0, KV_EMPTY = 1, QD_FULL = 2, QD_EMPTY = 2 + NS,
+                       S_FULL = 2 + 2 * NS, P_FULL = S_FULL + 1, DP_FULL = S_FULL + 2,
+                       DS_FULL = S_FULL + 3, ACC_DONE = S_FULL + 4, DONE = S_FULL + 5,
+                       N_BARS = S_FULL + 6;
+  static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
+  static constexpr int ALLOC = MISC_OFF + 16 + 1024;
+  // tensor memory columns: S^T (P^T as bf16 over its first 64), dP^T (dS^T
+  // likewise), dv, dk
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + DH;
+  __host__ __device__ static constexpr bool per_warp(int i) { return i == P_FULL || i == DS_FULL; }
+};
+
+struct KvItem {
+  int b, kvh, t;
+};
+
+__device__ __forceinline__ KvItem kv_item(const BwdArgs& a, int x) {
+  const int groups = a.B * a.Hkv;
+  KvItem it;
+  it.t = x / groups;  // ascending: for causal the lowest key tiles carry the most queries
+  const int g = x % groups;
+  it.b = g / a.Hkv;
+  it.kvh = g % a.Hkv;
+  return it;
+}
+
+// (query head of the group, query tile) pairs of one dk/dv item, query tiles
+// ascending inside each head; causal skips query tiles before the key tile.
+struct KvCursor {
+  int hh, j, j0, tiles;
+  __device__ __forceinline__ void init(const BwdArgs& a, const KvItem& it) {
+    j0 = a.causal ? it.t : 0;
+    tiles = a.tiles;
+    hh = 0;
+    j = j0;
+  }
+  __device__ __forceinline__ void next() {
+    if (++j == tiles) {
+      j = j0;
+      ++hh;
+    }
+  }
+};
+
+__device__ __forceinline__ int kv_steps(const BwdArgs& a, const KvItem& it) {
+  return (a.H / a.Hkv) * (a.tiles - (a.causal ? it.t : 0));
+}
+
+template <int DH>
+__device__ void dkdv_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                         const CUtensorMap* tdo, const BwdArgs& a, uint32_t sbase,
+                         volatile int* abort_flag) {
+  using L = KvLayout<DH>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const uint64_t pol_keep = l2_policy_evict_last();
+  const uint64_t pol_once = l2_policy_evict_first();
+  const int G = a.H / a.Hkv;
+  uint32_t kv_cnt = 0, g = 0;
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    if (k * (int)gridDim.x >= a.n_items) break;
+    const int x = bwd_item_index(k);
+    if (x >= a.n_items) continue;
+    const KvItem it = kv_item(a, x);
+    const int ns = kv_steps(a, it);
+    if (kv_cnt > 0 && !bwait(bar(L::KV_EMPTY), (kv_cnt - 1) & 1, abort_flag, a)) break;
+    mbar_arrive_expect_tx(bar(L::KV_FULL), 2 * L::TILE);
+    const int krow = it.b * a.S + it.t * kT;
+    for (int kb = 0; kb < L::DK; ++kb) {
+      tma_load_3d(sbase + L::K_OFF + kb * kBlk, tk, bar(L::KV_FULL), kb * 64, it.kvh, krow, pol_once);
+      tma_load_3d(sbase + L::V_OFF + kb * kBlk, tv, bar(L::KV_FULL), kb * 64, it.kvh, krow, pol_once);
+    }
+    ++kv_cnt;
+    KvCursor cur;
+    cur.init(a, it);
+    for (int u = 0; u < ns; ++u, ++g, cur.next()) {
+      const int st = g % L::NS;
+      const uint32_t ph = (g / L::NS) & 1;
+      if (!bwait(bar(L::QD_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
+      const int h = it.kvh * G + cur.hh;
+      const int qrow = it.b * a.S + cur.j * kT;
+      const uint32_t stage = sbase + L::ST_OFF + st * L::STAGE;
+      const uint32_t fb = bar(L::QD_FULL + st);
+      mbar_arrive_expect_tx(fb, 2 * L::TILE + 1024);
+      for (int kb = 0; kb < L::DK; ++kb) {
+        tma_load_3d(stage + kb * kBlk, tq, fb, kb * 64, h, qrow, pol_keep);
+        tma_load_3d(stage + L::TILE + kb * kBlk, tdo, fb, kb * 64, h, qrow, pol_keep);
+      }
+      const size_t li = ((size_t)it.b * a.H + h) * a.S + (size_t)cur.j * kT;
+      bulk_load(stage + L::NL2_IN, a.nlse2 + li, 512, fb);
+      bulk_load(stage + L::DL_IN, a.ndelta + li, 512, fb);
+    }
+  }
+  if (!ok) {  // let the copies in flight land before shared memory goes away
+    if (kv_cnt > 0) wait_drain(bar(L::KV_FULL), (kv_cnt - 1) & 1, a.timeout_ns);
+    for (uint32_t c = (g > (uint32_t)L::NS ? g - L::NS : 0); c < g; ++c)
+      wait_drain(bar(L::QD_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
+  }
+}
+
+// Issue order per step u of an item (S^T = K Q^T, dP^T = V dO^T):
+//   dv += P^T(u) dO(u)      once P^T(u) is in tensor memory
+//   S^T(u+1)                right behind it (overwrites P^T(u); in-order pipe)
+//   dk += dS^T(u) Q(u)      once dS^T(u) is in tensor memory
+//   dP^T(u+1)               right behind it (overwrites dS^T(u))
+template <int DH>
+__device__ void dkdv_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
+                         volatile int* abort_flag) {
+  using L = KvLayout<DH>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const uint32_t tS = tmem + L::S_COL, tDP = tmem + L::DP_COL;
+  const uint32_t tDV = tmem + L::DV_COL, tDK = tmem + L::DK_COL;
+  const uint32_t k_lo = desc_lo(sbase + L::K_OFF, 16), v_lo = desc_lo(sbase + L::V_OFF, 16);
+  const uint32_t q_lo0 = desc_lo(sbase + L::ST_OFF, 16);
+  const uint32_t do_lo0 = desc_lo(sbase + L::ST_OFF + L::TILE, 16);
+  const uint32_t q_mn0 = desc_lo(sbase + L::ST_OFF, kBlk);
+  const uint32_t do_mn0 = desc_lo(sbase + L::ST_OFF + L::TILE, kBlk);
+  constexpr uint32_t kStageLo = (uint32_t)L::STAGE >> 4;
+  uint32_t kv_cnt = 0, g = 0;
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    if (k * (int)gridDim.x >= a.n_items) break;
+    const int x = bwd_item_index(k);
+    if (x >= a.n_items) continue;
+    const KvItem it = kv_item(a, x);
+    const int ns = kv_steps(a, it);
+    if (!bwait(bar(L::KV_FULL), kv_cnt & 1, abort_flag, a)) break;
+    ++kv_cnt;
+    {  // prologue: S^T(0), dP^T(0)
+      const int st = g % L::NS;
+      if (!bwait(bar(L::QD_FULL + st), (g / L::NS) & 1, abort_flag, a)) break;
+      tc_fence_after();
+      mma_nt<DH>(tS, k_lo, q_lo0 + st * kStageLo);
+      mma_commit(bar(L::S_FULL));
+      mma_nt<DH>(tDP, v_lo, do_lo0 + st * kStageLo);
+      mma_commit(bar(L::DP_FULL));
+    }
+    for (int u = 0; u < ns; ++u, ++g) {
+      const int st = g % L::NS, st1 = (g + 1) % L::NS;
+      const bool more = u + 1 < ns;
+      if (!bwait(bar(L::P_FULL), g & 1, abort_flag, a)) { ok = false; break; }
+      tc_fence_after();
+      mma_tn<DH>(tDV, tS, do_mn0 + st * kStageLo, u > 0);
+      if (more) {
+        if (!bwait(bar(L::QD_FULL + st1), ((g + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+        tc_fence_after();
+        mma_nt<DH>(tS, k_lo, q_lo0 + st1 * kStageLo);
+        mma_commit(bar(L::S_FULL));
+      }
+      if (!bwait(bar(L::DS_FULL), g & 1, abort_flag, a)) { ok = false; break; }
+      tc_fence_after();
+      mma_tn<DH>(tDK, tDP, q_mn0 + st * kStageLo, u > 0);
+      mma_commit(bar(L::QD_EMPTY + st));
+      if (more) {
+        mma_nt<DH>(tDP, v_lo, do_lo0 + st1 * kStageLo);
+        mma_commit(bar(L::DP_FULL));
+      }
+    }
+    if (!ok) break;
+    mma_commit(bar(L::ACC_DONE));
+    mma_commit(bar(L::KV_EMPTY));
+  }
+  mma_commit(bar(L::DONE));
+  wait_drain(bar(L::DONE), 0, a.timeout_ns);
+}
+
+template <int DH>
+__device__ void dkdv_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
+                             volatile int* abort_flag, const uint8_t* smem) {
+  using L = KvLayout<DH>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const int warp = threadIdx.x >> 5;
+  const int r = threadIdx.x;  // key row inside the tile == TMEM lane
+  const uint32_t lb = (uint32_t)(32 * warp) << 16;
+  const uint32_t tS = tmem + lb + L::S_COL, tDP = tmem + lb + L::DP_COL;
+  const uint32_t tDV = tmem + lb + L::DV_COL, tDK = tmem + lb + L::DK_COL;
+  const uint64_t c2 = f2_pack(a.scale_log2, a.scale_log2);
+  uint32_t g = 0, n_done = 0;
+  for (int k = 0;; ++k) {
+    if (k * (int)gridDim.x >= a.n_items) break;
+    const int x = bwd_item_index(k);
+    if (x >= a.n_items) continue;
+    const KvItem it = kv_item(a, x);
+    const int ns = kv_steps(a, it);
+    KvCursor cur;
+    cur.init(a, it);
+    for (int u = 0; u < ns; ++u, ++g, cur.next()) {
+      const uint8_t* stage = smem + L::ST_OFF + (g % L::NS) * L::STAGE;
+      const float* nl2 = reinterpret_cast<const float*>(stage + L::NL2_IN);
+      const float* dl = reinterpret_cast<const float*>(stage + L::DL_IN);
+      const bool diag = a.causal && cur.j == it.t;
+      // the per-column arrays arrived by bulk copy: acquire them through the
+      // stage's own barrier (already complete once S^T of this step exists)
+      if (!bwait_warp(bar(L::QD_FULL + g % L::NS), (g / L::NS) & 1, abort_flag, a)) return;
+      if (!bwait_warp(bar(L::S_FULL), g & 1, abort_flag, a)) return;
+      tc_fence_after();
+      uint32_t sa[32], sb[32], sc[32], sd[32];
+      tmem_ld32(tS + 0, sa);
+      tmem_ld32(tS + 32, sb);
+      tmem_ld32(tS + 64, sc);
+      tmem_ld32(tS + 96, sd);
+      tmem_wait_ld_regs(sa);
+      tmem_wait_ld_regs(sb);
+      tmem_wait_ld_regs(sc);
+      tmem_wait_ld_regs(sd);
+      // P^T: queries before this key row are masked on the diagonal tile
+      uint32_t pk[16];
+      if (diag) {
+        exp_chunk<true, true>(sa, 0, r, c2, 0, nl2);
+        exp_chunk<true, true>(sb, 32, r, c2, 0, nl2);
+        exp_chunk<true, true>(sc, 64, r, c2, 0, nl2);
+        exp_chunk<true, true>(sd, 96, r, c2, 0, nl2);
+      } else {
+        exp_chunk<false, true>(sa, 0, r, c2, 0, nl2);
+        exp_chunk<false, true>(sb, 32, r, c2, 0, nl2);
+        exp_chunk<false, true>(sc, 64, r, c2, 0, nl2);
+        exp_chunk<false, true>(sd, 96, r, c2, 0, nl2);
+      }
+      pack_chunk(sa, pk);
+      tmem_st16(tS + 0, pk);
+      pack_chunk(sb, pk);
+      tmem_st16(tS + 16, pk);
+      pack_chunk(sc, pk);
+      tmem_st16(tS + 32, pk);
+      pack_chunk(sd, pk);
+      tmem_st16(tS + 48, pk);
+      tmem_wait_st();
+      warp_arrive(bar(L::P_FULL));
+
+      // dS^T = P^T (dP^T - delta), written over the consumed dP^T columns
+      if (!bwait_warp(bar(L::DP_FULL), g & 1, abort_flag, a)) return;
+      tc_fence_after();
+      uint32_t va[32], vb[32];
+      tmem_ld32(tDP + 0, va);
+      tmem_wait_ld_regs(va);
+      tmem_ld32(tDP + 32, vb);
+      ds_chunk(sa, va, 0, 0, dl, pk);
+      tmem_st16(tDP + 0, pk);
+      tmem_wait_ld_regs(vb);
+      tmem_ld32(tDP + 64, va);
+      ds_chunk(sb, vb, 32, 0, dl, pk);
+      tmem_st16(tDP + 16, pk);
+      tmem_wait_ld_regs(va);
+      tmem_ld32(tDP + 96, vb);
+      ds_chunk(sc, va, 64, 0, dl, pk);
+      tmem_st16(tDP + 32, pk);
+      tmem_wait_ld_regs(vb);
+      ds_chunk(sd, vb, 96, 0, dl, pk);
+      tmem_st16(tDP + 48, pk);
+      tmem_wait_st();
+      warp_arrive(bar(L::DS_FULL));
+    }
+    // epilogue: dv and dk rows of this key
+    if (!bwait_warp(bar(L::ACC_DONE), n_done & 1, abort_flag, a)) return;
+    ++n_done;
+    tc_fence_after();
+    const size_t row = ((size_t)it.b * a.S + (size_t)it.t * kT + r) * a.Hkv + it.kvh;
+    store_row<DH>(tDV, 1.0f, static_cast<__nv_bfloat16*>(a.dv) + row * DH);
+    store_row<DH>(tDK, a.scale, static_cast<__nv_bfloat16*>(a.dk) + row * DH);
+    tc_fence_before();
+  }
+}
+
+// ================================================================== dq
+template <int DH>
+struct DqLayout {
+  static constexpr int DK = DH / 64;
+  static constexpr int NS = (DH == 128) ? 2 : 4;  // K/V ring depth
+  static constexpr int TILE = kT * DH * 2;
+  static constexpr int Q_OFF = 0, DO_OFF = TILE, K_OFF = 2 * TILE;
+  static constexpr int V_OFF = K_OFF + NS * TILE;
+  static constexpr int BAR_OFF = V_OFF + NS * TILE;
+  static constexpr int QD_FULL = 0, QD_EMPTY = 1, K_FULL = 2, K_EMPTY = 2 + NS,
+                       V_FULL = 2 + 2 * NS, V_EMPTY = 2 + 3 * NS, S_FULL = 2 + 4 * NS,
+                       S_FREE = S_FULL + 1, DP_FULL = S_FULL + 2, DP_FREE = S_FULL + 3,
+                       DS_FULL = S_FULL + 4, DQ_DONE = S_FULL + 5, DONE = S_FULL + 6,
+                       N_BARS = S_FULL + 7;
+  static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
+  static constexpr int ALLOC = MISC_OFF + 16 + 1024;
+  // tensor memory columns: S, dP, dS (bf16 pairs), dq
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DS_COL = 256, DQ_COL = 320;
+  __host__ __device__ static constexpr bool per_warp(int i) {
+    return i == S_FREE || i == DP_FREE || i == DS_FULL;
+  }
+};
+
+struct DqItem {
+  int b, h, kvh, j;
+};
+
+__device__ __forceinline__ DqItem dq_item(const BwdArgs& a, int x) {
+  const int groups = a.B * a.H;
+  const int qi = x / groups, g = x % groups;
+  DqItem it;
+  it.j = a.causal ? a.tiles - 1 - qi : qi;  // causal: heaviest rows first
+  it.b = g / a.H;
+  it.h = g % a.H;
+  it.kvh = it.h / (a.H / a.Hkv);
+  return it;
+}
+
+// Key tiles of one query tile in the forward's ring order: its own chunk
+// first (up to the diagonal tile when causal), then the chunks below it,
+// wrapping around for non-causal.
+struct RingCursor {
+  int kt, left, c, tpc, P;
+  __device__ __forceinline__ void init(const BwdArgs& a, int j) {
+    tpc = a.tpc;
+    P = a.P;
+    c = j / tpc;
+    kt = c * tpc;
+    left = a.causal ? j - kt + 1 : tpc;
+  }
+  __device__ __forceinline__ void next() {
+    if (--left > 0) {
+      ++kt;
+      return;
+    }
+    c = (c == 0) ? P - 1 : c - 1;
+    kt = c * tpc;
+    left = tpc;
+  }
+};
+
+template <int DH>
+__device__ void dq_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                       const CUtensorMap* tdo, const BwdArgs& a, uint32_t sbase,
+                       volatile int* abort_flag) {
+  using L = DqLayout<DH>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const uint64_t pol_kv = l2_policy_evict_last();
+  const uint64_t pol_q = l2_policy_evict_first();
+  uint32_t qd_cnt = 0, kv_cnt = 0;
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    if (k * (int)gridDim.x >= a.n_items) break;
+    const int x = bwd_item_index(k);
+    if (x >= a.n_items) continue;
+    const DqItem it = dq_item(a, x);
+    const int ns = a.causal ? it.j + 1 : a.tiles;
+    if (qd_cnt > 0 && !bwait(bar(L::QD_EMPTY), (qd_cnt - 1) & 1, abort_flag, a)) break;
+    mbar_arrive_expect_tx(bar(L::QD_FULL), 2 * L::TILE);
+    const int qrow = it.b * a.S + it.j * kT;
+    for (int kb = 0; kb < L::DK; ++kb) {
+      tma_load_3d(sbase + L::Q_OFF + kb * kBlk, tq, bar(L::QD_FULL), kb * 64, it.h, qrow, pol_q);
+      tma_load_3d(sbase + L::DO_OFF + kb * kBlk, tdo, bar(L::QD_FULL), kb * 64, it.h, qrow, pol_q);
+    }
+    ++qd_cnt;
+    RingCursor cur;
+    cur.init(a, it.j);
+    for (int u = 0; u < ns; ++u, ++kv_cnt, cur.next()) {
+      const int st = kv_cnt % L::NS;
+      const uint32_t ph = (kv_cnt / L::NS) & 1;
+      const int row = it.b * a.S + cur.kt * kT;
+      if (!bwait(bar(L::K_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
+      mbar_arrive_expect_tx(bar(L::K_FULL + st), L::TILE);
+      for (int kb = 0; kb < L::DK; ++kb)
+        tma_load_3d(sbase + L::K_OFF + st * L::TILE + kb * kBlk, tk, bar(L::K_FULL + st), kb * 64,
+                    it.kvh, row, pol_kv);
+      if (!bwait(bar(L::V_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
+      mbar_arrive_expect_tx(bar(L::V_FULL + st), L::TILE);
+      for (int kb = 0; kb < L::DK; ++kb)
+        tma_load_3d(sbase + L::V_OFF + st * L::TILE + kb * kBlk, tv, bar(L::V_FULL + st), kb * 64,
+                    it.kvh, row, pol_kv);
+    }
+  }
+  if (!ok) {
+    if (qd_cnt > 0) wait_drain(bar(L::QD_FULL), (qd_cnt - 1) & 1, a.timeout_ns);
+    for (uint32_t c = (kv_cnt > (uint32_t)L::NS ? kv_cnt - L::NS : 0); c < kv_cnt; ++c) {
+      wait_drain(bar(L::K_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
+      wait_drain(bar(L::V_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
+    }
+  }
+}
+
+// Issue order per step u of an item (S = Q K^T, dP = dO V^T):
+//   S(u+1)     once the elementwise warps have read S(u) into registers
+//   dP(u+1)    once they have read dP(u)
+//   dq += dS(u) K(u)   once dS(u) is in tensor memory
+// so S and dP of the next step run on the tensor cores while the elementwise
+// warps work on the current one.
+template <int DH>
+__device__ void dq_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
+  using L = DqLayout<DH>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const uint32_t tS = tmem + L::S_COL, tDP = tmem + L::DP_COL;
+  const uint32_t tDS = tmem + L::DS_COL, tDQ = tmem + L::DQ_COL;
+  const uint32_t q_lo = desc_lo(sbase + L::Q_OFF, 16), do_lo = desc_lo(sbase + L::DO_OFF, 16);
+  const uint32_t k_lo0 = desc_lo(sbase + L::K_OFF, 16), v_lo0 = desc_lo(sbase + L::V_OFF, 16);
+  const uint32_t k_mn0 = desc_lo(sbase + L::K_OFF, kBlk);  // K as the MN-major B of dq += dS K
+  constexpr uint32_t kStageLo = (uint32_t)L::TILE >> 4;
+  uint32_t qd_cnt = 0, c = 0, g = 0;
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    if (k * (int)gridDim.x >= a.n_items) break;
+    const int x = bwd_item_index(k);
+    if (x >= a.n_items) continue;
+    const DqItem it = dq_item(a, x);
+    const int ns = a.causal ? it.j + 1 : a.tiles;
+    if (!bwait(bar(L::QD_FULL), qd_cnt & 1, abort_flag, a)) break;
+    ++qd_cnt;
+    {  // prologue: S(0), dP(0), once the previous item's last S and dP are read
+      const int st = c % L::NS;
+      const uint32_t ph = (c / L::NS) & 1;
+      if (g > 0 && !bwait(bar(L::S_FREE), (g - 1) & 1, abort_flag, a)) break;
+      if (!bwait(bar(L::K_FULL + st), ph, abort_flag, a)) break;
+      tc_fence_after();
+      mma_nt<DH>(tS, q_lo, k_lo0 + st * kStageLo);
+      mma_commit(bar(L::S_FULL));
+      if (g > 0 && !bwait(bar(L::DP_FREE), (g - 1) & 1, abort_flag, a)) break;
+      if (!bwait(bar(L::V_FULL + st), ph, abort_flag, a)) break;
+      tc_fence_after();
+      mma_nt<DH>(tDP, do_lo, v_lo0 + st * kStageLo);
+      mma_commit(bar(L::DP_FULL));
+      mma_commit(bar(L::V_EMPTY + st));
+      if (ns == 1) mma_commit(bar(L::QD_EMPTY));
+    }
+    for (int u = 0; u < ns; ++u, ++g, ++c) {
+      const int st = c % L::NS, st1 = (c + 1) % L::NS;
+      const uint32_t ph1 = ((c + 1) / L::NS) & 1;
+      if (u + 1 < ns) {
+        if (!bwait(bar(L::S_FREE), g & 1, abort_flag, a)) { ok = false; break; }
+        if (!bwait(bar(L::K_FULL + st1), ph1, abort_flag, a)) { ok = false; break; }
+        tc_fence_after();
+        mma_nt<DH>(tS, q_lo, k_lo0 + st1 * kStageLo);
+        mma_commit(bar(L::S_FULL));
+        if (!bwait(bar(L::DP_FREE), g & 1, abort_flag, a)) { ok = false; break; }
+        if (!bwait(bar(L::V_FULL + st1), ph1, abort_flag, a)) { ok = false; break; }
+        tc_fence_after();
+        mma_nt<DH>(tDP, do_lo, v_lo0 + st1 * kStageLo);
+        mma_commit(bar(L::DP_FULL));
+        mma_commit(bar(L::V_EMPTY + st1));
+        if (u + 2 == ns) mma_commit(bar(L::QD_EMPTY));  // last reads of q and dout issued
+      }
+      if (!bwait(bar(L::DS_FULL), g & 1, abort_flag, a)) { ok = false; break; }
+      tc_fence_after();
+      mma_tn<DH>(tDQ, tDS, k_mn0 + st * kStageLo, u > 0);
+      mma_commit(bar(L::DQ_DONE));
+      mma_commit(bar(L::K_EMPTY + st));
+    }
+  }
+  mma_commit(bar(L::DONE));
+  wait_drain(bar(L::DONE), 0, a.timeout_ns);
+}
+
+template <int DH>
+__device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
+                           volatile int* abort_flag) {
+  using L = DqLayout<DH>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const int warp = threadIdx.x >> 5;
+  const int r = threadIdx.x;  // query row inside the tile == TMEM lane
+  const uint32_t lb = (uint32_t)(32 * warp) << 16;
+  const uint32_t tS = tmem + lb + L::S_COL, tDP = tmem + lb + L::DP_COL;
+  const uint32_t tDS = tmem + lb + L::DS_COL, tDQ = tmem + lb + L::DQ_COL;
+  const uint64_t c2 = f2_pack(a.scale_log2, a.scale_log2);
+  uint32_t g = 0;
+  for (int k = 0;; ++k) {
+    if (k * (int)gridDim.x >= a.n_items) break;
+    const int x = bwd_item_index(k);
+    if (x >= a.n_items) continue;
+    const DqItem it = dq_item(a, x);
+    const int ns = a.causal ? it.j + 1 : a.tiles;
+    const size_t li = ((size_t)it.b * a.H + it.h) * a.S + (size_t)it.j * kT + r;
+    const float nl2 = a.nlse2[li], ndl = a.ndelta[li];
+    const uint64_t nl2x2 = f2_pack(nl2, nl2), ndl2 = f2_pack(ndl, ndl);
+    RingCursor cur;
+    cur.init(a, it.j);
+    for (int u = 0; u < ns; ++u, ++g, cur.next()) {
+      const bool diag = a.causal && cur.kt == it.j;
+      if (!bwait_warp(bar(L::S_FULL), g & 1, abort_flag, a)) return;
+      tc_fence_after();
+      uint32_t sa[32], sb[32], sc[32], sd[32];
+      tmem_ld32(tS + 0, sa);
+      tmem_ld32(tS + 32, sb);
+      tmem_ld32(tS + 64, sc);
+      tmem_ld32(tS + 96, sd);
+      tmem_wait_ld_regs(sa);
+      tmem_wait_ld_regs(sb);
+      tmem_wait_ld_regs(sc);
+      tmem_wait_ld_regs(sd);
+      warp_arrive(bar(L::S_FREE));
+      // P: keys past this query row are masked on the diagonal tile
+      if (diag) {
+        exp_chunk<true, false>(sa, 0, r, c2, nl2x2, nullptr);
+        exp_chunk<true, false>(sb, 32, r, c2, nl2x2, nullptr);
+        exp_chunk<true, false>(sc, 64, r, c2, nl2x2, nullptr);
+        exp_chunk<true, false>(sd, 96, r, c2, nl2x2, nullptr);
+      } else {
+        exp_chunk<false, false>(sa, 0, r, c2, nl2x2, nullptr);
+        exp_chunk<false, false>(sb, 32, r, c2, nl2x2, nullptr);
+        exp_chunk<false, false>(sc, 64, r, c2, nl2x2, nullptr);
+        exp_chunk<false, false>(sd, 96, r, c2, nl2x2, nullptr);
+      }
+      if (!bwait_warp(bar(L::DP_FULL), g & 1, abort_flag, a)) return;
+      // the previous step's dq MMA has read the dS columns
+      if (g > 0 && !bwait_warp(bar(L::DQ_DONE), (g - 1) & 1, abort_flag, a)) return;
+      tc_fence_after();
+      uint32_t va[32], vb[32], pk[16];
+      tmem_ld32(tDP + 0, va);
+      tmem_wait_ld_regs(va);
+      tmem_ld32(tDP + 32, vb);
+      ds_chunk(sa, va, 0, ndl2, nullptr, pk);
+      tmem_st16(tDS + 0, pk);
+      tmem_wait_ld_regs(vb);
+      tmem_ld32(tDP + 64, va);
+      ds_chunk(sb, vb, 32, ndl2, nullptr, pk);
+      tmem_st16(tDS + 16, pk);
+      tmem_wait_ld_regs(va);
+      tmem_ld32(tDP + 96, vb);
+      ds_chunk(sc, va, 64, ndl2, nullptr, pk);
+      tmem_st16(tDS + 32, pk);
+      tmem_wait_ld_regs(vb);
+      warp_arrive(bar(L::DP_FREE));
+      ds_chunk(sd, vb, 96, ndl2, nullptr, pk);
+      tmem_st16(tDS + 48, pk);
+      tmem_wait_st();
+      warp_arrive(bar(L::DS_FULL));
+    }
+    // epilogue: dq row = scale * accumulator
+    if (!bwait_warp(bar(L::DQ_DONE), (g - 1) & 1, abort_flag, a)) return;
+    tc_fence_after();
+    const size_t row = ((size_t)it.b * a.S + (size_t)it.j * kT + r) * a.H + it.h;
+    store_row<DH>(tDQ, a.scale, static_cast<__nv_bfloat16*>(a.dq) + row * DH);
+    tc_fence_before();
+  }
+}
+
+// ============================================================ kernels
+template <class L>
+__device__ __forceinline__ void init_barriers(uint32_t sbase, volatile int* abort_flag) {
+  for (int i = 0; i < L::N_BARS; ++i) mbar_init(sbase + L::BAR_OFF + 8u * i, L::per_warp(i) ? 4u : 1u);
+  *abort_flag = 0;
+  fence_barrier_init();
+  fence_proxy_async_smem();
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const BwdArgs a) {
+  using L = KvLayout<DH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+  if (threadIdx.x == 0) init_barriers<L>(sbase, abort_flag);
+  if (warp == kBwdWarpTma && (threadIdx.x & 31) == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+  }
+  if (warp == kBwdWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  if (warp < 4)
+    dkdv_compute<DH>(a, sbase, tmem, abort_flag, smem);
+  else if (warp == kBwdWarpTma && (threadIdx.x & 31) == 0)
+    dkdv_tma<DH>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, abort_flag);
+  else if (warp == kBwdWarpMma && (threadIdx.x & 31) == 0)
+    dkdv_mma<DH>(a, sbase, tmem, abort_flag);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kBwdWarpMma) {
+    __syncwarp();
+    tmem_dealloc(tmem, kBwdTmemCols);
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdArgs a) {
+  using L = DqLayout<DH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::MISC_OFF + 4);
+  if (threadIdx.x == 0) init_barriers<L>(sbase, abort_flag);
+  if (warp == kBwdWarpTma && (threadIdx.x & 31) == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+  }
+  if (warp == kBwdWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  if (warp < 4)
+    dq_compute<DH>(a, sbase, tmem, abort_flag);
+  else if (warp == kBwdWarpTma && (threadIdx.x & 31) == 0)
+    dq_tma<DH>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, abort_flag);
+  else if (warp == kBwdWarpMma && (threadIdx.x & 31) == 0)
+    dq_mma<DH>(a, sbase, tmem, abort_flag);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kBwdWarpMma) {
+    __syncwarp();
+    tmem_dealloc(tmem, kBwdTmemCols);
+  }
+}
+
+template <class Kernel>
+cudaError_t launch_tc(Kernel kernel, int smem, int grid, cudaStream_t stream, const CUtensorMap& tq,
+                      const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                      const BwdArgs& args) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(int D, const BwdArgs& args, int grid, cudaStream_t stream) {
+  if (D == 128)
+    bwd_prep_kernel<128><<<grid, 256, 0, stream>>>(args);
+  else
+    bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
+                            int grid, cudaStream_t stream) {
+  if (D == 128)
+    return launch_tc(bwd_dkdv_kernel<128>, KvLayout<128>::ALLOC, grid, stream, tq, tk, tv, tdo, args);
+  return launch_tc(bwd_dkdv_kernel<64>, KvLayout<64>::ALLOC, grid, stream, tq, tk, tv, tdo, args);
+}
+
+cudaError_t launch_bwd_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
+                          int grid, cudaStream_t stream) {
+  if (D == 128)
+    return launch_tc(bwd_dq_kernel<128>, DqLayout<128>::ALLOC, grid, stream, tq, tk, tv, tdo, args);
+  return launch_tc(bwd_dq_kernel<64>, DqLayout<64>::ALLOC, grid, stream, tq, tk, tv, tdo, args);
+}
+
+}  // namespace ra

@@ -39,6 +39,7 @@
 
 #include "ra_internal.h"
 #include "ra_ptx.cuh"
+#include "ra_umma.cuh"
 
 namespace ra {
 
@@ -87,13 +88,6 @@ struct Layout {
   __host__ __device__ static constexpr uint32_t S_COL(int i) { return 128u * i; }
   __host__ __device__ static constexpr uint32_t O_COL(int i) { return 256u + (uint32_t)D * i; }
 };
-
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
-// B K-major (0) or MN-major (1), shape M x N.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
 
 struct Item {
   int b, kvh;
@@ -206,35 +200,10 @@ __device__ __forceinline__ bool is_diag(const FwdArgs& a, const Item& it, int sl
   return a.causal && a.k_tile0 + kt == a.q_tile0 + it.qt[slot];
 }
 
-// Bounded wait on one mbarrier phase (single thread).
-__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       unsigned long long timeout_ns, unsigned int* status) {
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
-    if ((it & 3u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > timeout_ns) {
-        if (status) atomicOr(status, kStatusTimeout);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, const FwdArgs& a) {
   if (mbar_try_wait(bar, parity)) return true;
   return wait_slow(bar, parity, abort_flag, a.timeout_ns, a.status);
-}
-
-// Bounded wait used while tearing down after an abort: never raises the flag
-// again and gives up after at most 100 ms.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long t) {
-  volatile int never = 0;
-  if (!mbar_try_wait(bar, parity))
-    wait_slow(bar, parity, &never, t < 100000000ull ? t : 100000000ull, nullptr);
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the warp follows its verdict.
@@ -325,12 +294,6 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 // issuing thread keeps the work between consecutive MMAs to a few integer
 // operations: descriptors are precomputed halves plus immediate offsets, and
 // the step sequence comes from a division-free cursor.
-__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
-  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
-}
-// high word of a 128-byte-swizzle descriptor: stride byte offset 1024 B
-// (8 rows of 128 B), descriptor version 1, swizzle mode 128 B
-constexpr uint32_t kDescHiSw128 = ((1024u >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {

@@ -38,6 +38,27 @@ struct FwdArgs {
   int strict_mma_order;  // 1: wait for O_i += P_i V to complete before S_i is rewritten
 };
 
+// Kernel arguments of the backward pass besides the tensor maps (q, k, v, dout).
+struct BwdArgs {
+  const void* out;       // bf16 [B,S,H,D] forward output (row-sum kernel only)
+  const void* dout;      // bf16 [B,S,H,D] gradient of the output
+  const float* lse;      // fp32 [B,H,S] from the forward (natural log)
+  float* nlse2;          // workspace fp32 [B,H,S]: -lse * log2(e)
+  float* ndelta;         // workspace fp32 [B,H,S]: -sum_d out * dout
+  void* dq;              // bf16 [B,S,H,D]
+  void* dk;              // bf16 [B,S,Hkv,D]
+  void* dv;              // bf16 [B,S,Hkv,D]
+  unsigned int* status;  // this device's sticky status word
+  int B, H, Hkv, S, P;
+  int causal;
+  int tiles;             // S / 128
+  int tpc;               // 128-row tiles per ring chunk (S / P / 128)
+  int n_items;           // work items of the kernel being launched
+  float scale;           // multiplies dq and dk
+  float scale_log2;      // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
 // status word bits
 constexpr unsigned int kStatusTimeout = 1u;
 
@@ -47,6 +68,15 @@ cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
 size_t fwd_smem_bytes(int D);
 cudaError_t status_word_ptr(unsigned int** p);
 cudaError_t read_and_clear_status(unsigned int* value);
+
+// ra_bwd.cu
+cudaError_t launch_bwd_prep(int D, const BwdArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
+                            int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
+                          int grid, cudaStream_t stream);
 
 // ra_merge.cu
 cudaError_t launch_merge(const void* o_parts, int o_is_fp32, const float* lse_parts, int n,

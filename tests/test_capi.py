@@ -19,7 +19,8 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for n in ("ra_fwd", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string"):
+    for n in ("ra_fwd", "ra_merge_partials", "ra_bwd", "ra_bwd_workspace_bytes",
+              "ra_get_last_device_status", "ra_status_string"):
         assert n in names
 
 
@@ -33,7 +34,7 @@ def test_status_strings(ralib):
     assert ralib.ra_status_string(0) == "RA_OK"
     assert ralib.ra_status_string(4) == "RA_ERR_TIMEOUT"
     assert ralib.ra_status_string(99) == "RA_ERR_UNKNOWN"
-    assert ralib.ra_version() == (0 << 16) | (1 << 8)
+    assert ralib.ra_version() == (0 << 16) | (2 << 8)
 
 
 # Fake, 16-byte aligned addresses: validation must reject these calls before
@@ -92,4 +93,31 @@ def test_block_validation_rejects_before_launch(ralib, kw, code):
     lib = ralib._load()
     rc = lib.ra_fwd_block(a["q"], a["k"], a["v"], a["o"], a["l"], a["B"], a["H"], a["Hkv"], a["Sq"],
                           a["Sk"], a["D"], a["qp"], a["kp"], a["causal"], a["scale"], None)
+    assert rc == code
+
+
+def test_bwd_workspace_bytes(ralib):
+    assert ralib.ra_bwd_workspace_bytes(2, 32, 16384) == 8 * 2 * 32 * 16384
+    assert ralib.ra_bwd_workspace_bytes(0, 4, 128) == 0
+    assert ralib.ra_bwd_workspace_bytes(1, -1, 128) == 0
+
+
+W = 0x60000
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(lse=0), 1), (dict(dout=0), 1), (dict(dq=0), 1), (dict(dk=0), 1),
+    (dict(dv=0), 1), (dict(ws=0), 1), (dict(B=0), 1), (dict(P=3), 1), (dict(H=3, Hkv=2), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(ws_bytes=8 * 4 * 256 - 16), 1),    # one row short of 8*B*H*S
+    (dict(scale=-0.1), 2), (dict(D=96), 2), (dict(S=384, P=2, ws_bytes=8 * 4 * 384), 2),
+    (dict(dq=O + 8), 2), (dict(ws=W + 4), 2), (dict(lse=L + 2), 2),
+])
+def test_bwd_validation_rejects_before_launch(ralib, kw, code):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, dout=Q + 0x100000, dq=O + 0x100000, dk=K + 0x100000,
+             dv=V + 0x100000, ws=W, ws_bytes=8 * 4 * 256, B=1, H=4, Hkv=2, S=256, D=128, P=2,
+             causal=1, scale=0.125)
+    a.update(kw)
+    lib = ralib._load()
+    rc = lib.ra_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dout"], a["dq"], a["dk"], a["dv"],
+                    a["ws"], a["ws_bytes"], a["B"], a["H"], a["Hkv"], a["S"], a["D"], a["P"],
+                    a["causal"], a["scale"], None)
     assert rc == code
