@@ -258,6 +258,50 @@ def measure_merge(ra, w, flush, stream, steps: int = 20):
             "unit": "GB/s", "frac": gbs / float(peaks["hbm_gbs"]), "peak_source": f"{src} copy"}
 
 
+def measure_bwd(ra, w, flush, stream, qd, kd, vd, out, lse, steps: int = 10):
+    """Time ra_bwd (row sums, dk/dv and dq kernels) on the workload, given the
+    forward's out and lse and a seeded N(0,1) output gradient.  FLOPs follow
+    the usual count of a backward pass, five GEMM-shaped products per allowed
+    (query, key) pair (S, dP, dV, dK, dQ: 2.5x the forward's); the kernels
+    execute seven (S and dP are recomputed by the dk/dv and the dq kernel),
+    reported as ``executed_tflops``."""
+    import torch
+
+    g = torch.Generator(device="cuda")
+    g.manual_seed(101)
+    dout = torch.randn(qd.shape, generator=g, device="cuda").to(torch.bfloat16)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(ra.ra_bwd_workspace_bytes(w.B, w.H, w.S), dtype=torch.uint8, device="cuda")
+
+    def call():
+        ra.ra_bwd(qd, kd, vd, out, lse, dout, P=w.P, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
+                  dv=dv, workspace=ws, stream=stream)
+
+    for _ in range(3):
+        call()
+    ts = []
+    for _ in range(steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    if ra.ra_get_last_device_status() != 0:
+        raise RuntimeError("device status reported a timeout in the backward")
+    ms = statistics.mean(ts)
+    flops = 2.5 * w.flops
+    tflops = flops / (ms * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    del dout, dq, dk, dv, ws
+    return {"kernels": "bwd_prep + bwd_dkdv + bwd_dq (ra_bwd)", "launches_per_step": 3,
+            "ms": ms, "flops": flops, "bound": "tensor", "achieved": tflops, "peak": peak,
+            "unit": "TFLOP/s", "frac": tflops / peak, "executed_tflops": 1.4 * tflops,
+            "peak_source": f"{src} bf16 dense burst"}
+
+
 def run_ours(args):
     import torch
 
@@ -344,6 +388,7 @@ def run_ours(args):
     e2e_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in e2e_evs[1:])
 
     merge = None if args.no_merge else measure_merge(ra, w, flush, stream)
+    bwd = None if args.no_bwd else measure_bwd(ra, w, flush, stream, qd, kd, vd, out, lse)
 
     # slowest rank decides
     if ws > 1:
@@ -389,6 +434,7 @@ def run_ours(args):
                           "max": max(kernel_ms)},
             "kernel_sha": kernel_sha(),
             "merge": merge,
+            "bwd": bwd,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -407,6 +453,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-merge", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
