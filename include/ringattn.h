@@ -163,6 +163,32 @@ ra_status ra_bwd(const void* q, const void* k, const void* v, const void* out, c
                  int causal, float scale, void* stream);
 
 /*
+ * ra_bwd_static -- ra_bwd without a caller workspace, for callers that must
+ * not allocate device memory per call.  (No counterpart on the pages: an
+ * allocation-free form of this library's ra_bwd.)
+ *
+ * The per-row scratch (-lse*log2(e) and -delta, 8 bytes per query row) lives
+ * in one fixed device array inside the library: 16 MiB, enough for
+ * B*H*S <= 2^21 = 2,097,152 query rows.  Its address is looked up once per
+ * device, when the library first sets that device up.  The call allocates
+ * nothing (no cudaMalloc/cudaFree, no allocating library routine) and the
+ * scratch needs no clearing: the first kernel writes every value the other
+ * two read.
+ *
+ * Every call on a device shares that one array: two ra_bwd_static calls that
+ * can run at the same time (on different streams, or from different host
+ * threads) race on it and can return wrong gradients.  Issue them on one
+ * stream, or use ra_bwd with a workspace per stream.
+ *
+ * Arguments, layouts, results and errors as ra_bwd without the workspace,
+ * plus RA_ERR_UNSUPPORTED when B*H*S exceeds 2^21.
+ */
+ra_status ra_bwd_static(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                        int H, int Hkv, int S, int D, int P, int causal, float scale,
+                        void* stream);
+
+/*
  * ra_get_last_device_status -- synchronise `stream`, then read and clear this
  * device's sticky status word.  Returns RA_ERR_TIMEOUT if any kernel launched
  * since the previous query gave up a bounded wait (its outputs are then not

@@ -20,7 +20,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+__all__ = ["ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
            "ra_debug_set_fault", "ra_set_mma_order", "ra_shutdown", "ra_version", "RaError", "library_path",
            "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT"]
 
@@ -30,7 +30,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libringattn.so")
 _lib = None
 
-EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
            "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_set_mma_order",
            "ra_shutdown")
 
@@ -65,6 +65,8 @@ def _load():
     lib.ra_bwd_workspace_bytes.restype = ull
     lib.ra_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ull, i, i, i, i, i, i, i, f, vp]
     lib.ra_bwd.restype = i
+    lib.ra_bwd_static.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.ra_bwd_static.restype = i
     lib.ra_merge_partials.argtypes = [vp, i, vp, i, vp, vp, i, i, i, i, vp]
     lib.ra_merge_partials.restype = i
     lib.ra_get_last_device_status.argtypes = [vp]
@@ -212,6 +214,37 @@ def ra_bwd(q, k, v, out, lse, dout, *, P: int, causal: bool, scale: float | None
                       workspace.data_ptr(), workspace.numel() * workspace.element_size(), B, H, Hkv,
                       S, D, int(P), int(bool(causal)), float(scale), _stream_ptr(stream))
     _check(code, "ra_bwd")
+    return dq, dk, dv
+
+
+def ra_bwd_static(q, k, v, out, lse, dout, dq, dk, dv, *, P: int, causal: bool,
+                  scale: float | None = None, stream=None):
+    """:func:`ra_bwd` on the library's fixed scratch (no workspace, no
+    allocation in the call; calls that can overlap race on that scratch).
+    The caller passes the output buffers ``dq``, ``dk``, ``dv``."""
+    import torch
+
+    lib = _load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
+                 (dk, "dk"), (dv, "dv")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{n} must be a contiguous 4-D bf16 CUDA tensor")
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if (tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != tuple(k.shape)
+            or tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape)
+            or tuple(dq.shape) != tuple(q.shape) or tuple(dk.shape) != tuple(k.shape)
+            or tuple(dv.shape) != tuple(k.shape)):
+        raise ValueError("shapes must match ra_bwd's")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [B,H,S] fp32 tensor")
+    if scale is None:
+        scale = D ** -0.5
+    code = lib.ra_bwd_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                             dv.data_ptr(), B, H, Hkv, S, D, int(P), int(bool(causal)),
+                             float(scale), _stream_ptr(stream))
+    _check(code, "ra_bwd_static")
     return dq, dk, dv
 
 

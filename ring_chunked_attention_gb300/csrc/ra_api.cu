@@ -32,6 +32,7 @@ struct DeviceInfo {
   bool sm103 = false;
   int sms = 0;
   unsigned int* status = nullptr;
+  float* bwd_scratch = nullptr;  // the static scratch of ra_bwd_static on this device
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -51,9 +52,12 @@ ra_status device_info(DeviceInfo** out) {
       return cuda_fail(e);
     unsigned int* st = nullptr;
     if ((e = ra::status_word_ptr(&st)) != cudaSuccess) return cuda_fail(e);
+    float* scratch = nullptr;
+    if ((e = ra::bwd_static_scratch(&scratch)) != cudaSuccess) return cuda_fail(e);
     d.sm103 = (major == 10 && minor == 3);
     d.sms = sms;
     d.status = st;
+    d.bwd_scratch = scratch;
     d.valid = true;
   }
   *out = &d;
@@ -277,30 +281,37 @@ unsigned long long ra_bwd_workspace_bytes(int B, int H, int S) {
   return (unsigned long long)B * (unsigned long long)H * (unsigned long long)S * 8ull;
 }
 
-ra_status ra_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                 const void* dout, void* dq, void* dk, void* dv, void* workspace,
-                 unsigned long long workspace_bytes, int B, int H, int Hkv, int S, int D, int P,
-                 int causal, float scale, void* stream) {
-  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
-    return RA_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Checks shared by ra_bwd and ra_bwd_static (everything but the workspace).
+ra_status check_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int S,
+                    int D, int P, float scale) {
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return RA_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || P <= 0) return RA_ERR_INVALID_ARG;
   if (H % Hkv != 0 || S % P != 0) return RA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return RA_ERR_INVALID_ARG;
-  if (workspace_bytes < ra_bwd_workspace_bytes(B, H, S)) return RA_ERR_INVALID_ARG;
   if (scale < 0.0f) return RA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
   if ((S / P) % 128 != 0) return RA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return RA_ERR_UNSUPPORTED;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return RA_ERR_UNSUPPORTED;
   if ((long long)B * S >= (1ll << 31) || (long long)B * H * (S / 128) >= (1ll << 31))
     return RA_ERR_UNSUPPORTED;
+  return RA_OK;
+}
 
-  DeviceInfo* dev = nullptr;
-  ra_status st = device_info(&dev);
-  if (st != RA_OK) return st;
-  if (!dev->sm103) return RA_ERR_UNSUPPORTED;
+// Tensor maps, arguments and the three launches of the backward, with the
+// per-row scratch at `ws` (8*B*H*S bytes).  Arguments are already checked.
+ra_status launch_backward(DeviceInfo* dev, const void* q, const void* k, const void* v,
+                          const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                          void* dv, float* ws, int B, int H, int Hkv, int S, int D, int P,
+                          int causal, float scale, void* stream) {
+  ra_status st;
   CUtensorMap tq, tk, tv, tdo;
   if ((st = tensor_map(q, (long long)B * S, H, D, &tq)) != RA_OK) return st;
   if ((st = tensor_map(k, (long long)B * S, Hkv, D, &tk)) != RA_OK) return st;
@@ -312,7 +323,7 @@ ra_status ra_bwd(const void* q, const void* k, const void* v, const void* out, c
   a.out = out;
   a.dout = dout;
   a.lse = lse;
-  a.nlse2 = static_cast<float*>(workspace);
+  a.nlse2 = ws;
   a.ndelta = a.nlse2 + (size_t)B * H * S;
   a.dq = dq;
   a.dk = dk;
@@ -345,6 +356,39 @@ ra_status ra_bwd(const void* q, const void* k, const void* v, const void* out, c
   e = ra::launch_bwd_dq(D, tq, tk, tv, tdo, a, a.n_items < dev->sms ? a.n_items : dev->sms, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ra_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                 unsigned long long workspace_bytes, int B, int H, int Hkv, int S, int D, int P,
+                 int causal, float scale, void* stream) {
+  ra_status st = check_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, H, Hkv, S, D, P, scale);
+  if (st != RA_OK) return st;
+  if (!workspace || workspace_bytes < ra_bwd_workspace_bytes(B, H, S)) return RA_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return RA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != RA_OK) return st;
+  if (!dev->sm103) return RA_ERR_UNSUPPORTED;
+  return launch_backward(dev, q, k, v, out, lse, dout, dq, dk, dv, static_cast<float*>(workspace),
+                         B, H, Hkv, S, D, P, causal, scale, stream);
+}
+
+ra_status ra_bwd_static(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                        int H, int Hkv, int S, int D, int P, int causal, float scale,
+                        void* stream) {
+  ra_status st = check_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, H, Hkv, S, D, P, scale);
+  if (st != RA_OK) return st;
+  if ((long long)B * H * S > ra::kStaticBwdRows) return RA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != RA_OK) return st;
+  if (!dev->sm103) return RA_ERR_UNSUPPORTED;
+  return launch_backward(dev, q, k, v, out, lse, dout, dq, dk, dv, dev->bwd_scratch, B, H, Hkv, S,
+                         D, P, causal, scale, stream);
 }
 
 ra_status ra_get_last_device_status(void* stream) {

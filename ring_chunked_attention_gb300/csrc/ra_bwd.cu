@@ -864,6 +864,17 @@ cudaError_t launch_tc(Kernel kernel, int smem, int grid, cudaStream_t stream, co
 
 }  // namespace
 
+// Scratch of the allocation-free backward entry point: -lse*log2(e) and
+// -delta for up to kStaticBwdRows query rows (16 MiB), in the same
+// [B,H,S] + [B,H,S] layout as a caller's workspace.  Every call on a device
+// shares it; nothing in it needs clearing (the row-sum kernel writes every
+// value the other two kernels read).
+static __device__ __align__(256) float g_bwd_scratch[2 * kStaticBwdRows];
+
+cudaError_t bwd_static_scratch(float** p) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_bwd_scratch);
+}
+
 cudaError_t launch_bwd_prep(int D, const BwdArgs& args, int grid, cudaStream_t stream) {
   if (D == 128)
     bwd_prep_kernel<128><<<grid, 256, 0, stream>>>(args);

@@ -70,6 +70,8 @@ cudaError_t status_word_ptr(unsigned int** p);
 cudaError_t read_and_clear_status(unsigned int* value);
 
 // ra_bwd.cu
+constexpr long long kStaticBwdRows = 1ll << 21;  // query rows B*H*S of the static scratch
+cudaError_t bwd_static_scratch(float** p);       // its device address (cudaGetSymbolAddress)
 cudaError_t launch_bwd_prep(int D, const BwdArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
