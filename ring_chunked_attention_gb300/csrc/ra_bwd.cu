@@ -28,10 +28,17 @@
 // exchange for no fp32 dq scratch and no atomic traffic.
 //
 // CTA organisation of both tensor-core kernels (one persistent CTA per SM):
-//   warps 0-3  elementwise work, one thread per TMEM lane (query row in the
-//              dq kernel, key row in the dk/dv kernel), and the epilogue
-//   warp  4    TMA producer
-//   warp  5    MMA issuer (one thread)
+//   warps 0-3  elementwise work on columns 0-63 of every tile row, one
+//              thread per TMEM lane (query row in the dq kernel, key row in
+//              the dk/dv kernel), and half of the epilogue
+//   warps 4-7  the same for columns 64-127 (nothing in the backward's
+//              elementwise work reduces across a row, so the halves never
+//              exchange data)
+//   warp  8    TMA producer
+//   warp  9    MMA issuer (one thread)
+//   warps 10-11 idle (they complete the producer warpgroup)
+// Registers are split with setmaxnreg as in the forward kernel: 168 per
+// thread at launch, 200 for the elementwise warpgroups, 104 for the rest.
 // Every wait is bounded as in the forward kernel: on timeout the CTA sets the
 // status word, drains its copies and MMAs, frees tensor memory and exits.
 #include <cuda.h>
@@ -47,9 +54,14 @@
 namespace ra {
 namespace {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdWarpTma = 4;
-constexpr int kBwdWarpMma = 5;
+constexpr int kBwdThreads = 384;     // warps 10-11 idle: they complete the producer warpgroup
+constexpr int kBwdComputeWarps = 8;  // two warpgroups, one half of every row each
+constexpr int kBwdWarpTma = 8;
+constexpr int kBwdWarpMma = 9;
+// setmaxnreg split of the 168 registers a thread gets at launch
+constexpr uint32_t kBwdLaunchRegs = 168, kBwdComputeRegs = 200, kBwdProducerRegs = 104;
+static_assert(2 * 128 * kBwdComputeRegs + 128 * kBwdProducerRegs == kBwdThreads * kBwdLaunchRegs,
+              "register split must use exactly the launch allocation");
 constexpr int kT = 128;                // rows per tile (queries or keys)
 constexpr int kBlk = 128 * 128;        // one [128 rows x 64 cols] bf16 block
 constexpr uint32_t kBwdTmemCols = 512;
@@ -68,14 +80,19 @@ __device__ __forceinline__ void mma_nt(uint32_t tD, uint32_t a_lo, uint32_t b_lo
 }
 
 // D[128 x DH] (+)= A[128 x 128] (bf16 pairs in tensor memory) * B[128 x DH]
-// (an MN-major tile in shared memory).
-template <int DH>
+// (an MN-major tile in shared memory).  The A operand's K = 128 columns are
+// 64 packed columns: contiguous at tA when kSplitA is false; otherwise the
+// first 32 at tA and the last 32 at tA + 64 (each half of the elementwise
+// work packs its 64 columns inside its own 64-column half of the source).
+template <int DH, bool kSplitA>
 __device__ __forceinline__ void mma_tn(uint32_t tD, uint32_t tA, uint32_t b_lo, bool accumulate) {
   constexpr uint32_t idesc = make_idesc(kT, DH, 1);
 #pragma unroll
-  for (int kk = 0; kk < kT / 16; ++kk)
-    mma_ts_lh(tD, tA + kk * 8, b_lo + (uint32_t)(kk * (2048 >> 4)), kDescHiSw128, idesc,
+  for (int kk = 0; kk < kT / 16; ++kk) {
+    const uint32_t a_col = kSplitA ? (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8) : (uint32_t)(kk * 8);
+    mma_ts_lh(tD, tA + a_col, b_lo + (uint32_t)(kk * (2048 >> 4)), kDescHiSw128, idesc,
               (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
 // ------------------------------------------------------------- waits
@@ -93,7 +110,7 @@ __device__ __forceinline__ bool bwait_warp(uint32_t bar, uint32_t parity,
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// all four warps of the elementwise warpgroup arrive once each
+// every elementwise warp arrives once
 __device__ __forceinline__ void warp_arrive(uint32_t bar) {
   tc_fence_before();
   __syncwarp();
@@ -156,13 +173,13 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&p)[32], const uint32_t
   }
 }
 
-// D fp32 accumulator columns of this thread's TMEM lane -> bf16 row in global
-// memory, times `mul`.
-template <int DH>
+// NC fp32 accumulator columns of this thread's TMEM lane -> bf16 in global
+// memory at dst, times `mul`.
+template <int NC>
 __device__ __forceinline__ void store_row(uint32_t tAcc, float mul, __nv_bfloat16* dst) {
   uint4* row = reinterpret_cast<uint4*>(dst);
 #pragma unroll 1
-  for (int c0 = 0; c0 < DH; c0 += 32) {
+  for (int c0 = 0; c0 < NC; c0 += 32) {
     uint32_t o[32];
     tmem_ld32(tAcc + c0, o);
     tmem_wait_ld_regs(o);
@@ -230,15 +247,16 @@ struct KvLayout {
   static constexpr int NL2_IN = 2 * TILE, DL_IN = 2 * TILE + 512;  // offsets inside a stage
   static constexpr int BAR_OFF = ST_OFF + NS * STAGE;
   static constexpr int KV_FULL = 0, KV_EMPTY = 1, QD_FULL = 2, QD_EMPTY = 2 + NS,
-                       S_FULL = 2 + 2 * NS, P_FULL = S_FULL + 1, DP_FULL = S_FULL + 2,
-                       DS_FULL = S_FULL + 3, ACC_DONE = S_FULL + 4, DONE = S_FULL + 5,
+                       S_FULL = 2 + 2 * NS, S_FREE = S_FULL + 1, DP_FULL = S_FULL + 2,
+                       PDS_FULL = S_FULL + 3, ACC_DONE = S_FULL + 4, DONE = S_FULL + 5,
                        N_BARS = S_FULL + 6;
   static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
   static constexpr int ALLOC = MISC_OFF + 16 + 1024;
-  // tensor memory columns: S^T (P^T as bf16 over its first 64), dP^T (dS^T
-  // likewise), dv, dk
+  // tensor memory columns: S^T, dP^T (then P^T and dS^T as bf16 pairs: in
+  // each 64-column half, P^T in the first 32 columns and dS^T in the last
+  // 32), dv, dk
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + DH;
-  __host__ __device__ static constexpr bool per_warp(int i) { return i == P_FULL || i == DS_FULL; }
+  __host__ __device__ static constexpr bool per_warp(int i) { return i == S_FREE || i == PDS_FULL; }
 };
 
 struct KvItem {
@@ -330,10 +348,11 @@ __device__ void dkdv_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 }
 
 // Issue order per step u of an item (S^T = K Q^T, dP^T = V dO^T):
-//   dv += P^T(u) dO(u)      once P^T(u) is in tensor memory
-//   S^T(u+1)                right behind it (overwrites P^T(u); in-order pipe)
-//   dk += dS^T(u) Q(u)      once dS^T(u) is in tensor memory
-//   dP^T(u+1)               right behind it (overwrites dS^T(u))
+//   S^T(u+1)            once the elementwise warps have read S^T(u)
+//   dv += P^T(u) dO(u)  once P^T(u) and dS^T(u) are in tensor memory (both in
+//   dk += dS^T(u) Q(u)  the dP^T columns)
+//   dP^T(u+1)           right behind them (overwrites P^T(u), dS^T(u); in-order pipe)
+// so the next S^T runs on the tensor cores while the warps work on this step.
 template <int DH>
 __device__ void dkdv_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
                          volatile int* abort_flag) {
@@ -357,9 +376,10 @@ __device__ void dkdv_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
     const int ns = kv_steps(a, it);
     if (!bwait(bar(L::KV_FULL), kv_cnt & 1, abort_flag, a)) break;
     ++kv_cnt;
-    {  // prologue: S^T(0), dP^T(0)
+    {  // prologue: S^T(0), dP^T(0), once the previous step's S^T has been read
       const int st = g % L::NS;
       if (!bwait(bar(L::QD_FULL + st), (g / L::NS) & 1, abort_flag, a)) break;
+      if (g > 0 && !bwait(bar(L::S_FREE), (g - 1) & 1, abort_flag, a)) break;
       tc_fence_after();
       mma_nt<DH>(tS, k_lo, q_lo0 + st * kStageLo);
       mma_commit(bar(L::S_FULL));
@@ -369,18 +389,17 @@ __device__ void dkdv_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
     for (int u = 0; u < ns; ++u, ++g) {
       const int st = g % L::NS, st1 = (g + 1) % L::NS;
       const bool more = u + 1 < ns;
-      if (!bwait(bar(L::P_FULL), g & 1, abort_flag, a)) { ok = false; break; }
-      tc_fence_after();
-      mma_tn<DH>(tDV, tS, do_mn0 + st * kStageLo, u > 0);
       if (more) {
+        if (!bwait(bar(L::S_FREE), g & 1, abort_flag, a)) { ok = false; break; }
         if (!bwait(bar(L::QD_FULL + st1), ((g + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
         mma_nt<DH>(tS, k_lo, q_lo0 + st1 * kStageLo);
         mma_commit(bar(L::S_FULL));
       }
-      if (!bwait(bar(L::DS_FULL), g & 1, abort_flag, a)) { ok = false; break; }
+      if (!bwait(bar(L::PDS_FULL), g & 1, abort_flag, a)) { ok = false; break; }
       tc_fence_after();
-      mma_tn<DH>(tDK, tDP, q_mn0 + st * kStageLo, u > 0);
+      mma_tn<DH, true>(tDV, tDP, do_mn0 + st * kStageLo, u > 0);
+      mma_tn<DH, true>(tDK, tDP + 32, q_mn0 + st * kStageLo, u > 0);
       mma_commit(bar(L::QD_EMPTY + st));
       if (more) {
         mma_nt<DH>(tDP, v_lo, do_lo0 + st1 * kStageLo);
@@ -401,9 +420,10 @@ __device__ void dkdv_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
   using L = KvLayout<DH>;
   auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
   const int warp = threadIdx.x >> 5;
-  const int r = threadIdx.x;  // key row inside the tile == TMEM lane
-  const uint32_t lb = (uint32_t)(32 * warp) << 16;
-  const uint32_t tS = tmem + lb + L::S_COL, tDP = tmem + lb + L::DP_COL;
+  const int r = threadIdx.x & 127;   // key row inside the tile == TMEM lane
+  const int c0 = (warp >> 2) * 64;   // this warpgroup's half of the query columns
+  const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+  const uint32_t tS = tmem + lb + L::S_COL + c0, tDP = tmem + lb + L::DP_COL + c0;
   const uint32_t tDV = tmem + lb + L::DV_COL, tDK = tmem + lb + L::DK_COL;
   const uint64_t c2 = f2_pack(a.scale_log2, a.scale_log2);
   uint32_t g = 0, n_done = 0;
@@ -425,69 +445,48 @@ __device__ void dkdv_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (!bwait_warp(bar(L::QD_FULL + g % L::NS), (g / L::NS) & 1, abort_flag, a)) return;
       if (!bwait_warp(bar(L::S_FULL), g & 1, abort_flag, a)) return;
       tc_fence_after();
-      uint32_t sa[32], sb[32], sc[32], sd[32];
+      uint32_t sa[32], sb[32];
       tmem_ld32(tS + 0, sa);
       tmem_ld32(tS + 32, sb);
-      tmem_ld32(tS + 64, sc);
-      tmem_ld32(tS + 96, sd);
       tmem_wait_ld_regs(sa);
       tmem_wait_ld_regs(sb);
-      tmem_wait_ld_regs(sc);
-      tmem_wait_ld_regs(sd);
+      warp_arrive(bar(L::S_FREE));
       // P^T: queries before this key row are masked on the diagonal tile
-      uint32_t pk[16];
       if (diag) {
-        exp_chunk<true, true>(sa, 0, r, c2, 0, nl2);
-        exp_chunk<true, true>(sb, 32, r, c2, 0, nl2);
-        exp_chunk<true, true>(sc, 64, r, c2, 0, nl2);
-        exp_chunk<true, true>(sd, 96, r, c2, 0, nl2);
+        exp_chunk<true, true>(sa, c0, r, c2, 0, nl2);
+        exp_chunk<true, true>(sb, c0 + 32, r, c2, 0, nl2);
       } else {
-        exp_chunk<false, true>(sa, 0, r, c2, 0, nl2);
-        exp_chunk<false, true>(sb, 32, r, c2, 0, nl2);
-        exp_chunk<false, true>(sc, 64, r, c2, 0, nl2);
-        exp_chunk<false, true>(sd, 96, r, c2, 0, nl2);
+        exp_chunk<false, true>(sa, c0, r, c2, 0, nl2);
+        exp_chunk<false, true>(sb, c0 + 32, r, c2, 0, nl2);
       }
-      pack_chunk(sa, pk);
-      tmem_st16(tS + 0, pk);
-      pack_chunk(sb, pk);
-      tmem_st16(tS + 16, pk);
-      pack_chunk(sc, pk);
-      tmem_st16(tS + 32, pk);
-      pack_chunk(sd, pk);
-      tmem_st16(tS + 48, pk);
-      tmem_wait_st();
-      warp_arrive(bar(L::P_FULL));
-
-      // dS^T = P^T (dP^T - delta), written over the consumed dP^T columns
+      // dS^T = P^T (dP^T - delta).  This half's 64 dP^T columns, once read,
+      // take P^T (first 32) and dS^T (last 32) as bf16 pairs.
       if (!bwait_warp(bar(L::DP_FULL), g & 1, abort_flag, a)) return;
       tc_fence_after();
-      uint32_t va[32], vb[32];
+      uint32_t va[32], vb[32], pk[16];
       tmem_ld32(tDP + 0, va);
-      tmem_wait_ld_regs(va);
       tmem_ld32(tDP + 32, vb);
-      ds_chunk(sa, va, 0, 0, dl, pk);
-      tmem_st16(tDP + 0, pk);
-      tmem_wait_ld_regs(vb);
-      tmem_ld32(tDP + 64, va);
-      ds_chunk(sb, vb, 32, 0, dl, pk);
-      tmem_st16(tDP + 16, pk);
       tmem_wait_ld_regs(va);
-      tmem_ld32(tDP + 96, vb);
-      ds_chunk(sc, va, 64, 0, dl, pk);
-      tmem_st16(tDP + 32, pk);
       tmem_wait_ld_regs(vb);
-      ds_chunk(sd, vb, 96, 0, dl, pk);
+      pack_chunk(sa, pk);
+      tmem_st16(tDP + 0, pk);
+      pack_chunk(sb, pk);
+      tmem_st16(tDP + 16, pk);
+      ds_chunk(sa, va, c0, 0, dl, pk);
+      tmem_st16(tDP + 32, pk);
+      ds_chunk(sb, vb, c0 + 32, 0, dl, pk);
       tmem_st16(tDP + 48, pk);
       tmem_wait_st();
-      warp_arrive(bar(L::DS_FULL));
+      warp_arrive(bar(L::PDS_FULL));
     }
-    // epilogue: dv and dk rows of this key
+    // epilogue: this warpgroup's half of the dv and dk rows of this key
     if (!bwait_warp(bar(L::ACC_DONE), n_done & 1, abort_flag, a)) return;
     ++n_done;
     tc_fence_after();
     const size_t row = ((size_t)it.b * a.S + (size_t)it.t * kT + r) * a.Hkv + it.kvh;
-    store_row<DH>(tDV, 1.0f, static_cast<__nv_bfloat16*>(a.dv) + row * DH);
-    store_row<DH>(tDK, a.scale, static_cast<__nv_bfloat16*>(a.dk) + row * DH);
+    const int e0 = (warp >> 2) * (DH / 2);
+    store_row<DH / 2>(tDV + e0, 1.0f, static_cast<__nv_bfloat16*>(a.dv) + row * DH + e0);
+    store_row<DH / 2>(tDK + e0, a.scale, static_cast<__nv_bfloat16*>(a.dk) + row * DH + e0);
     tc_fence_before();
   }
 }
@@ -496,13 +495,17 @@ __device__ void dkdv_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
 template <int DH>
 struct DqLayout {
   static constexpr int DK = DH / 64;
-  static constexpr int NS = (DH == 128) ? 2 : 4;  // K/V ring depth
+  // K is read by the first and the last MMA of a step (S and dq), V only by
+  // the second (dP), so the K ring is one stage deeper than the V ring
+  static constexpr int NV = (DH == 128) ? 2 : 4;
+  static constexpr int NK = NV + 1;
   static constexpr int TILE = kT * DH * 2;
   static constexpr int Q_OFF = 0, DO_OFF = TILE, K_OFF = 2 * TILE;
-  static constexpr int V_OFF = K_OFF + NS * TILE;
-  static constexpr int BAR_OFF = V_OFF + NS * TILE;
-  static constexpr int QD_FULL = 0, QD_EMPTY = 1, K_FULL = 2, K_EMPTY = 2 + NS,
-                       V_FULL = 2 + 2 * NS, V_EMPTY = 2 + 3 * NS, S_FULL = 2 + 4 * NS,
+  static constexpr int V_OFF = K_OFF + NK * TILE;
+  static constexpr int BAR_OFF = V_OFF + NV * TILE;
+  static constexpr int QD_FULL = 0, QD_EMPTY = 1, K_FULL = 2, K_EMPTY = 2 + NK,
+                       V_FULL = 2 + 2 * NK, V_EMPTY = 2 + 2 * NK + NV,
+                       S_FULL = 2 + 2 * NK + 2 * NV,
                        S_FREE = S_FULL + 1, DP_FULL = S_FULL + 2, DP_FREE = S_FULL + 3,
                        DS_FULL = S_FULL + 4, DQ_DONE = S_FULL + 5, DONE = S_FULL + 6,
                        N_BARS = S_FULL + 7;
@@ -580,27 +583,26 @@ __device__ void dq_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
     RingCursor cur;
     cur.init(a, it.j);
     for (int u = 0; u < ns; ++u, ++kv_cnt, cur.next()) {
-      const int st = kv_cnt % L::NS;
-      const uint32_t ph = (kv_cnt / L::NS) & 1;
+      const int sk = kv_cnt % L::NK, sv = kv_cnt % L::NV;
       const int row = it.b * a.S + cur.kt * kT;
-      if (!bwait(bar(L::K_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
-      mbar_arrive_expect_tx(bar(L::K_FULL + st), L::TILE);
+      if (!bwait(bar(L::K_EMPTY + sk), ((kv_cnt / L::NK) & 1) ^ 1, abort_flag, a)) { ok = false; break; }
+      mbar_arrive_expect_tx(bar(L::K_FULL + sk), L::TILE);
       for (int kb = 0; kb < L::DK; ++kb)
-        tma_load_3d(sbase + L::K_OFF + st * L::TILE + kb * kBlk, tk, bar(L::K_FULL + st), kb * 64,
+        tma_load_3d(sbase + L::K_OFF + sk * L::TILE + kb * kBlk, tk, bar(L::K_FULL + sk), kb * 64,
                     it.kvh, row, pol_kv);
-      if (!bwait(bar(L::V_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
-      mbar_arrive_expect_tx(bar(L::V_FULL + st), L::TILE);
+      if (!bwait(bar(L::V_EMPTY + sv), ((kv_cnt / L::NV) & 1) ^ 1, abort_flag, a)) { ok = false; break; }
+      mbar_arrive_expect_tx(bar(L::V_FULL + sv), L::TILE);
       for (int kb = 0; kb < L::DK; ++kb)
-        tma_load_3d(sbase + L::V_OFF + st * L::TILE + kb * kBlk, tv, bar(L::V_FULL + st), kb * 64,
+        tma_load_3d(sbase + L::V_OFF + sv * L::TILE + kb * kBlk, tv, bar(L::V_FULL + sv), kb * 64,
                     it.kvh, row, pol_kv);
     }
   }
   if (!ok) {
     if (qd_cnt > 0) wait_drain(bar(L::QD_FULL), (qd_cnt - 1) & 1, a.timeout_ns);
-    for (uint32_t c = (kv_cnt > (uint32_t)L::NS ? kv_cnt - L::NS : 0); c < kv_cnt; ++c) {
-      wait_drain(bar(L::K_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
-      wait_drain(bar(L::V_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
-    }
+    for (uint32_t c = (kv_cnt > (uint32_t)L::NK ? kv_cnt - L::NK : 0); c < kv_cnt; ++c)
+      wait_drain(bar(L::K_FULL + c % L::NK), (c / L::NK) & 1, a.timeout_ns);
+    for (uint32_t c = (kv_cnt > (uint32_t)L::NV ? kv_cnt - L::NV : 0); c < kv_cnt; ++c)
+      wait_drain(bar(L::V_FULL + c % L::NV), (c / L::NV) & 1, a.timeout_ns);
   }
 }
 
@@ -631,43 +633,42 @@ __device__ void dq_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem, volatile
     if (!bwait(bar(L::QD_FULL), qd_cnt & 1, abort_flag, a)) break;
     ++qd_cnt;
     {  // prologue: S(0), dP(0), once the previous item's last S and dP are read
-      const int st = c % L::NS;
-      const uint32_t ph = (c / L::NS) & 1;
+      const int sk = c % L::NK, sv = c % L::NV;
       if (g > 0 && !bwait(bar(L::S_FREE), (g - 1) & 1, abort_flag, a)) break;
-      if (!bwait(bar(L::K_FULL + st), ph, abort_flag, a)) break;
+      if (!bwait(bar(L::K_FULL + sk), (c / L::NK) & 1, abort_flag, a)) break;
       tc_fence_after();
-      mma_nt<DH>(tS, q_lo, k_lo0 + st * kStageLo);
+      mma_nt<DH>(tS, q_lo, k_lo0 + sk * kStageLo);
       mma_commit(bar(L::S_FULL));
       if (g > 0 && !bwait(bar(L::DP_FREE), (g - 1) & 1, abort_flag, a)) break;
-      if (!bwait(bar(L::V_FULL + st), ph, abort_flag, a)) break;
+      if (!bwait(bar(L::V_FULL + sv), (c / L::NV) & 1, abort_flag, a)) break;
       tc_fence_after();
-      mma_nt<DH>(tDP, do_lo, v_lo0 + st * kStageLo);
+      mma_nt<DH>(tDP, do_lo, v_lo0 + sv * kStageLo);
       mma_commit(bar(L::DP_FULL));
-      mma_commit(bar(L::V_EMPTY + st));
+      mma_commit(bar(L::V_EMPTY + sv));
       if (ns == 1) mma_commit(bar(L::QD_EMPTY));
     }
     for (int u = 0; u < ns; ++u, ++g, ++c) {
-      const int st = c % L::NS, st1 = (c + 1) % L::NS;
-      const uint32_t ph1 = ((c + 1) / L::NS) & 1;
+      const int sk = c % L::NK;
       if (u + 1 < ns) {
+        const int sk1 = (c + 1) % L::NK, sv1 = (c + 1) % L::NV;
         if (!bwait(bar(L::S_FREE), g & 1, abort_flag, a)) { ok = false; break; }
-        if (!bwait(bar(L::K_FULL + st1), ph1, abort_flag, a)) { ok = false; break; }
+        if (!bwait(bar(L::K_FULL + sk1), ((c + 1) / L::NK) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
-        mma_nt<DH>(tS, q_lo, k_lo0 + st1 * kStageLo);
+        mma_nt<DH>(tS, q_lo, k_lo0 + sk1 * kStageLo);
         mma_commit(bar(L::S_FULL));
         if (!bwait(bar(L::DP_FREE), g & 1, abort_flag, a)) { ok = false; break; }
-        if (!bwait(bar(L::V_FULL + st1), ph1, abort_flag, a)) { ok = false; break; }
+        if (!bwait(bar(L::V_FULL + sv1), ((c + 1) / L::NV) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
-        mma_nt<DH>(tDP, do_lo, v_lo0 + st1 * kStageLo);
+        mma_nt<DH>(tDP, do_lo, v_lo0 + sv1 * kStageLo);
         mma_commit(bar(L::DP_FULL));
-        mma_commit(bar(L::V_EMPTY + st1));
+        mma_commit(bar(L::V_EMPTY + sv1));
         if (u + 2 == ns) mma_commit(bar(L::QD_EMPTY));  // last reads of q and dout issued
       }
       if (!bwait(bar(L::DS_FULL), g & 1, abort_flag, a)) { ok = false; break; }
       tc_fence_after();
-      mma_tn<DH>(tDQ, tDS, k_mn0 + st * kStageLo, u > 0);
+      mma_tn<DH, false>(tDQ, tDS, k_mn0 + sk * kStageLo, u > 0);
       mma_commit(bar(L::DQ_DONE));
-      mma_commit(bar(L::K_EMPTY + st));
+      mma_commit(bar(L::K_EMPTY + sk));
     }
   }
   mma_commit(bar(L::DONE));
@@ -680,10 +681,11 @@ __device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
   using L = DqLayout<DH>;
   auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
   const int warp = threadIdx.x >> 5;
-  const int r = threadIdx.x;  // query row inside the tile == TMEM lane
-  const uint32_t lb = (uint32_t)(32 * warp) << 16;
-  const uint32_t tS = tmem + lb + L::S_COL, tDP = tmem + lb + L::DP_COL;
-  const uint32_t tDS = tmem + lb + L::DS_COL, tDQ = tmem + lb + L::DQ_COL;
+  const int r = threadIdx.x & 127;  // query row inside the tile == TMEM lane
+  const int c0 = (warp >> 2) * 64;  // this warpgroup's half of the key columns
+  const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+  const uint32_t tS = tmem + lb + L::S_COL + c0, tDP = tmem + lb + L::DP_COL + c0;
+  const uint32_t tDS = tmem + lb + L::DS_COL + c0 / 2, tDQ = tmem + lb + L::DQ_COL;
   const uint64_t c2 = f2_pack(a.scale_log2, a.scale_log2);
   uint32_t g = 0;
   for (int k = 0;; ++k) {
@@ -701,27 +703,19 @@ __device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
       const bool diag = a.causal && cur.kt == it.j;
       if (!bwait_warp(bar(L::S_FULL), g & 1, abort_flag, a)) return;
       tc_fence_after();
-      uint32_t sa[32], sb[32], sc[32], sd[32];
+      uint32_t sa[32], sb[32];
       tmem_ld32(tS + 0, sa);
       tmem_ld32(tS + 32, sb);
-      tmem_ld32(tS + 64, sc);
-      tmem_ld32(tS + 96, sd);
       tmem_wait_ld_regs(sa);
       tmem_wait_ld_regs(sb);
-      tmem_wait_ld_regs(sc);
-      tmem_wait_ld_regs(sd);
       warp_arrive(bar(L::S_FREE));
       // P: keys past this query row are masked on the diagonal tile
       if (diag) {
-        exp_chunk<true, false>(sa, 0, r, c2, nl2x2, nullptr);
-        exp_chunk<true, false>(sb, 32, r, c2, nl2x2, nullptr);
-        exp_chunk<true, false>(sc, 64, r, c2, nl2x2, nullptr);
-        exp_chunk<true, false>(sd, 96, r, c2, nl2x2, nullptr);
+        exp_chunk<true, false>(sa, c0, r, c2, nl2x2, nullptr);
+        exp_chunk<true, false>(sb, c0 + 32, r, c2, nl2x2, nullptr);
       } else {
-        exp_chunk<false, false>(sa, 0, r, c2, nl2x2, nullptr);
-        exp_chunk<false, false>(sb, 32, r, c2, nl2x2, nullptr);
-        exp_chunk<false, false>(sc, 64, r, c2, nl2x2, nullptr);
-        exp_chunk<false, false>(sd, 96, r, c2, nl2x2, nullptr);
+        exp_chunk<false, false>(sa, c0, r, c2, nl2x2, nullptr);
+        exp_chunk<false, false>(sb, c0 + 32, r, c2, nl2x2, nullptr);
       }
       if (!bwait_warp(bar(L::DP_FULL), g & 1, abort_flag, a)) return;
       // the previous step's dq MMA has read the dS columns
@@ -729,30 +723,23 @@ __device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
       tc_fence_after();
       uint32_t va[32], vb[32], pk[16];
       tmem_ld32(tDP + 0, va);
-      tmem_wait_ld_regs(va);
       tmem_ld32(tDP + 32, vb);
-      ds_chunk(sa, va, 0, ndl2, nullptr, pk);
-      tmem_st16(tDS + 0, pk);
-      tmem_wait_ld_regs(vb);
-      tmem_ld32(tDP + 64, va);
-      ds_chunk(sb, vb, 32, ndl2, nullptr, pk);
-      tmem_st16(tDS + 16, pk);
       tmem_wait_ld_regs(va);
-      tmem_ld32(tDP + 96, vb);
-      ds_chunk(sc, va, 64, ndl2, nullptr, pk);
-      tmem_st16(tDS + 32, pk);
       tmem_wait_ld_regs(vb);
       warp_arrive(bar(L::DP_FREE));
-      ds_chunk(sd, vb, 96, ndl2, nullptr, pk);
-      tmem_st16(tDS + 48, pk);
+      ds_chunk(sa, va, c0, ndl2, nullptr, pk);
+      tmem_st16(tDS + 0, pk);
+      ds_chunk(sb, vb, c0 + 32, ndl2, nullptr, pk);
+      tmem_st16(tDS + 16, pk);
       tmem_wait_st();
       warp_arrive(bar(L::DS_FULL));
     }
-    // epilogue: dq row = scale * accumulator
+    // epilogue: this warpgroup's half of the dq row = scale * accumulator
     if (!bwait_warp(bar(L::DQ_DONE), (g - 1) & 1, abort_flag, a)) return;
     tc_fence_after();
     const size_t row = ((size_t)it.b * a.S + (size_t)it.j * kT + r) * a.H + it.h;
-    store_row<DH>(tDQ, a.scale, static_cast<__nv_bfloat16*>(a.dq) + row * DH);
+    const int e0 = (warp >> 2) * (DH / 2);
+    store_row<DH / 2>(tDQ + e0, a.scale, static_cast<__nv_bfloat16*>(a.dq) + row * DH + e0);
     tc_fence_before();
   }
 }
@@ -760,7 +747,8 @@ __device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
 // ============================================================ kernels
 template <class L>
 __device__ __forceinline__ void init_barriers(uint32_t sbase, volatile int* abort_flag) {
-  for (int i = 0; i < L::N_BARS; ++i) mbar_init(sbase + L::BAR_OFF + 8u * i, L::per_warp(i) ? 4u : 1u);
+  for (int i = 0; i < L::N_BARS; ++i)
+    mbar_init(sbase + L::BAR_OFF + 8u * i, L::per_warp(i) ? (uint32_t)kBwdComputeWarps : 1u);
   *abort_flag = 0;
   fence_barrier_init();
   fence_proxy_async_smem();
@@ -794,12 +782,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  if (warp < 4)
+  if (warp < kBwdComputeWarps) {
+    regs_inc<kBwdComputeRegs>();
     dkdv_compute<DH>(a, sbase, tmem, abort_flag, smem);
-  else if (warp == kBwdWarpTma && (threadIdx.x & 31) == 0)
-    dkdv_tma<DH>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, abort_flag);
-  else if (warp == kBwdWarpMma && (threadIdx.x & 31) == 0)
-    dkdv_mma<DH>(a, sbase, tmem, abort_flag);
+  } else {
+    regs_dec<kBwdProducerRegs>();
+    if (warp == kBwdWarpTma && (threadIdx.x & 31) == 0)
+      dkdv_tma<DH>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, abort_flag);
+    else if (warp == kBwdWarpMma && (threadIdx.x & 31) == 0)
+      dkdv_mma<DH>(a, sbase, tmem, abort_flag);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -837,12 +829,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  if (warp < 4)
+  if (warp < kBwdComputeWarps) {
+    regs_inc<kBwdComputeRegs>();
     dq_compute<DH>(a, sbase, tmem, abort_flag);
-  else if (warp == kBwdWarpTma && (threadIdx.x & 31) == 0)
-    dq_tma<DH>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, abort_flag);
-  else if (warp == kBwdWarpMma && (threadIdx.x & 31) == 0)
-    dq_mma<DH>(a, sbase, tmem, abort_flag);
+  } else {
+    regs_dec<kBwdProducerRegs>();
+    if (warp == kBwdWarpTma && (threadIdx.x & 31) == 0)
+      dq_tma<DH>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, abort_flag);
+    else if (warp == kBwdWarpMma && (threadIdx.x & 31) == 0)
+      dq_mma<DH>(a, sbase, tmem, abort_flag);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -856,7 +852,13 @@ template <class Kernel>
 cudaError_t launch_tc(Kernel kernel, int smem, int grid, cudaStream_t stream, const CUtensorMap& tq,
                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                       const BwdArgs& args) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // the setmaxnreg split is sized for exactly kBwdLaunchRegs registers per
+  // thread at launch; any other allocation would make setmaxnreg.inc wait forever
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != (int)kBwdLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, args);
   return cudaGetLastError();
