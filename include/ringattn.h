@@ -192,7 +192,11 @@ ra_status ra_bwd_static(const void* q, const void* k, const void* v, const void*
  * ra_get_last_device_status -- synchronise `stream`, then read and clear this
  * device's sticky status word.  Returns RA_ERR_TIMEOUT if any kernel launched
  * since the previous query gave up a bounded wait (its outputs are then not
- * valid), RA_ERR_CUDA if the synchronisation itself failed, else RA_OK.
+ * valid), RA_ERR_UNSUPPORTED if a kernel refused to run because the runtime
+ * gave it a shared-memory base that is not 1024-byte aligned (the dk/dv kernel
+ * of ra_bwd needs nearly all of a CTA's shared memory and cannot round the base
+ * up; its outputs are then not written), RA_ERR_CUDA if the synchronisation
+ * itself failed, else RA_OK.
  */
 ra_status ra_get_last_device_status(void* stream);
 

@@ -397,7 +397,8 @@ ra_status ra_get_last_device_status(void* stream) {
   unsigned int v = 0;
   e = ra::read_and_clear_status(&v);
   if (e != cudaSuccess) return cuda_fail(e);
-  return (v & ra::kStatusTimeout) ? RA_ERR_TIMEOUT : RA_OK;
+  if (v & ra::kStatusTimeout) return RA_ERR_TIMEOUT;
+  return (v & ra::kStatusLayout) ? RA_ERR_UNSUPPORTED : RA_OK;
 }
 
 const char* ra_status_string(ra_status s) {

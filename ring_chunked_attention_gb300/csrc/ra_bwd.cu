@@ -239,25 +239,35 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
 template <int DH>
 struct KvLayout {
   static constexpr int DK = DH / 64;
-  static constexpr int NS = (DH == 128) ? 2 : 4;  // q/dout ring depth
+  // q is read by the first MMA of a step (S^T) and by the last (dk); dout by
+  // the second and third, so the q ring is one stage deeper than the dout
+  // ring.  A dout stage also carries the step's 128 values of -lse*log2(e)
+  // and -delta (bulk copies); they are first read after S^T of the step.
+  static constexpr int ND = (DH == 128) ? 2 : 4;
+  static constexpr int NQ = ND + 1;
   static constexpr int TILE = kT * DH * 2;
-  static constexpr int K_OFF = 0, V_OFF = TILE;
-  static constexpr int STAGE = 2 * TILE + 1024;   // q, dout, -lse*log2e[128], -delta[128]
-  static constexpr int ST_OFF = 2 * TILE;
-  static constexpr int NL2_IN = 2 * TILE, DL_IN = 2 * TILE + 512;  // offsets inside a stage
-  static constexpr int BAR_OFF = ST_OFF + NS * STAGE;
-  static constexpr int KV_FULL = 0, KV_EMPTY = 1, QD_FULL = 2, QD_EMPTY = 2 + NS,
-                       S_FULL = 2 + 2 * NS, S_FREE = S_FULL + 1, DP_FULL = S_FULL + 2,
+  static constexpr int DSTAGE = TILE + 1024;
+  static constexpr int NL2_IN = TILE, DL_IN = TILE + 512;  // offsets inside a dout stage
+  static constexpr int K_OFF = 0, V_OFF = TILE, Q_OFF = 2 * TILE;
+  static constexpr int DO_OFF = Q_OFF + NQ * TILE;
+  static constexpr int BAR_OFF = DO_OFF + ND * DSTAGE;
+  static constexpr int KV_FULL = 0, KV_EMPTY = 1, Q_FULL = 2, Q_EMPTY = 2 + NQ,
+                       DO_FULL = 2 + 2 * NQ, DO_EMPTY = 2 + 2 * NQ + ND,
+                       S_FULL = 2 + 2 * NQ + 2 * ND, S_FREE = S_FULL + 1, DP_FULL = S_FULL + 2,
                        PDS_FULL = S_FULL + 3, ACC_DONE = S_FULL + 4, DONE = S_FULL + 5,
                        N_BARS = S_FULL + 6;
   static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
-  static constexpr int ALLOC = MISC_OFF + 16 + 1024;
+  // no alignment slack: at D = 128 this layout uses all but ~0.8 KB of the
+  // 227 KB a CTA can have, so the kernel requires (and checks) a 1024-byte
+  // aligned dynamic shared memory base instead of rounding it up
+  static constexpr int ALLOC = MISC_OFF + 16;
   // tensor memory columns: S^T, dP^T (then P^T and dS^T as bf16 pairs: in
   // each 64-column half, P^T in the first 32 columns and dS^T in the last
   // 32), dv, dk
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + DH;
   __host__ __device__ static constexpr bool per_warp(int i) { return i == S_FREE || i == PDS_FULL; }
 };
+static_assert(KvLayout<128>::ALLOC <= 232448, "dk/dv shared memory layout exceeds 227 KB");
 
 struct KvItem {
   int b, kvh, t;
@@ -323,18 +333,20 @@ __device__ void dkdv_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
     KvCursor cur;
     cur.init(a, it);
     for (int u = 0; u < ns; ++u, ++g, cur.next()) {
-      const int st = g % L::NS;
-      const uint32_t ph = (g / L::NS) & 1;
-      if (!bwait(bar(L::QD_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
+      const int sq = g % L::NQ, sd = g % L::ND;
       const int h = it.kvh * G + cur.hh;
       const int qrow = it.b * a.S + cur.j * kT;
-      const uint32_t stage = sbase + L::ST_OFF + st * L::STAGE;
-      const uint32_t fb = bar(L::QD_FULL + st);
-      mbar_arrive_expect_tx(fb, 2 * L::TILE + 1024);
-      for (int kb = 0; kb < L::DK; ++kb) {
-        tma_load_3d(stage + kb * kBlk, tq, fb, kb * 64, h, qrow, pol_keep);
-        tma_load_3d(stage + L::TILE + kb * kBlk, tdo, fb, kb * 64, h, qrow, pol_keep);
-      }
+      if (!bwait(bar(L::Q_EMPTY + sq), ((g / L::NQ) & 1) ^ 1, abort_flag, a)) { ok = false; break; }
+      mbar_arrive_expect_tx(bar(L::Q_FULL + sq), L::TILE);
+      for (int kb = 0; kb < L::DK; ++kb)
+        tma_load_3d(sbase + L::Q_OFF + sq * L::TILE + kb * kBlk, tq, bar(L::Q_FULL + sq), kb * 64,
+                    h, qrow, pol_keep);
+      if (!bwait(bar(L::DO_EMPTY + sd), ((g / L::ND) & 1) ^ 1, abort_flag, a)) { ok = false; break; }
+      const uint32_t stage = sbase + L::DO_OFF + sd * L::DSTAGE;
+      const uint32_t fb = bar(L::DO_FULL + sd);
+      mbar_arrive_expect_tx(fb, L::TILE + 1024);
+      for (int kb = 0; kb < L::DK; ++kb)
+        tma_load_3d(stage + kb * kBlk, tdo, fb, kb * 64, h, qrow, pol_keep);
       const size_t li = ((size_t)it.b * a.H + h) * a.S + (size_t)cur.j * kT;
       bulk_load(stage + L::NL2_IN, a.nlse2 + li, 512, fb);
       bulk_load(stage + L::DL_IN, a.ndelta + li, 512, fb);
@@ -342,8 +354,10 @@ __device__ void dkdv_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
   }
   if (!ok) {  // let the copies in flight land before shared memory goes away
     if (kv_cnt > 0) wait_drain(bar(L::KV_FULL), (kv_cnt - 1) & 1, a.timeout_ns);
-    for (uint32_t c = (g > (uint32_t)L::NS ? g - L::NS : 0); c < g; ++c)
-      wait_drain(bar(L::QD_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
+    for (uint32_t c = (g > (uint32_t)L::NQ ? g - L::NQ : 0); c < g; ++c)
+      wait_drain(bar(L::Q_FULL + c % L::NQ), (c / L::NQ) & 1, a.timeout_ns);
+    for (uint32_t c = (g > (uint32_t)L::ND ? g - L::ND : 0); c < g; ++c)
+      wait_drain(bar(L::DO_FULL + c % L::ND), (c / L::ND) & 1, a.timeout_ns);
   }
 }
 
@@ -361,11 +375,11 @@ __device__ void dkdv_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
   const uint32_t tS = tmem + L::S_COL, tDP = tmem + L::DP_COL;
   const uint32_t tDV = tmem + L::DV_COL, tDK = tmem + L::DK_COL;
   const uint32_t k_lo = desc_lo(sbase + L::K_OFF, 16), v_lo = desc_lo(sbase + L::V_OFF, 16);
-  const uint32_t q_lo0 = desc_lo(sbase + L::ST_OFF, 16);
-  const uint32_t do_lo0 = desc_lo(sbase + L::ST_OFF + L::TILE, 16);
-  const uint32_t q_mn0 = desc_lo(sbase + L::ST_OFF, kBlk);
-  const uint32_t do_mn0 = desc_lo(sbase + L::ST_OFF + L::TILE, kBlk);
-  constexpr uint32_t kStageLo = (uint32_t)L::STAGE >> 4;
+  const uint32_t q_lo0 = desc_lo(sbase + L::Q_OFF, 16);
+  const uint32_t do_lo0 = desc_lo(sbase + L::DO_OFF, 16);
+  const uint32_t q_mn0 = desc_lo(sbase + L::Q_OFF, kBlk);
+  const uint32_t do_mn0 = desc_lo(sbase + L::DO_OFF, kBlk);
+  constexpr uint32_t kQStageLo = (uint32_t)L::TILE >> 4, kDStageLo = (uint32_t)L::DSTAGE >> 4;
   uint32_t kv_cnt = 0, g = 0;
   bool ok = true;
   for (int k = 0; ok; ++k) {
@@ -377,32 +391,39 @@ __device__ void dkdv_mma(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
     if (!bwait(bar(L::KV_FULL), kv_cnt & 1, abort_flag, a)) break;
     ++kv_cnt;
     {  // prologue: S^T(0), dP^T(0), once the previous step's S^T has been read
-      const int st = g % L::NS;
-      if (!bwait(bar(L::QD_FULL + st), (g / L::NS) & 1, abort_flag, a)) break;
+      const int sq = g % L::NQ, sd = g % L::ND;
+      if (!bwait(bar(L::Q_FULL + sq), (g / L::NQ) & 1, abort_flag, a)) break;
       if (g > 0 && !bwait(bar(L::S_FREE), (g - 1) & 1, abort_flag, a)) break;
       tc_fence_after();
-      mma_nt<DH>(tS, k_lo, q_lo0 + st * kStageLo);
+      mma_nt<DH>(tS, k_lo, q_lo0 + sq * kQStageLo);
       mma_commit(bar(L::S_FULL));
-      mma_nt<DH>(tDP, v_lo, do_lo0 + st * kStageLo);
+      if (!bwait(bar(L::DO_FULL + sd), (g / L::ND) & 1, abort_flag, a)) break;
+      tc_fence_after();
+      mma_nt<DH>(tDP, v_lo, do_lo0 + sd * kDStageLo);
       mma_commit(bar(L::DP_FULL));
     }
     for (int u = 0; u < ns; ++u, ++g) {
-      const int st = g % L::NS, st1 = (g + 1) % L::NS;
+      const int sq = g % L::NQ, sd = g % L::ND;
       const bool more = u + 1 < ns;
       if (more) {
+        const int sq1 = (g + 1) % L::NQ;
         if (!bwait(bar(L::S_FREE), g & 1, abort_flag, a)) { ok = false; break; }
-        if (!bwait(bar(L::QD_FULL + st1), ((g + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+        if (!bwait(bar(L::Q_FULL + sq1), ((g + 1) / L::NQ) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
-        mma_nt<DH>(tS, k_lo, q_lo0 + st1 * kStageLo);
+        mma_nt<DH>(tS, k_lo, q_lo0 + sq1 * kQStageLo);
         mma_commit(bar(L::S_FULL));
       }
       if (!bwait(bar(L::PDS_FULL), g & 1, abort_flag, a)) { ok = false; break; }
       tc_fence_after();
-      mma_tn<DH, true>(tDV, tDP, do_mn0 + st * kStageLo, u > 0);
-      mma_tn<DH, true>(tDK, tDP + 32, q_mn0 + st * kStageLo, u > 0);
-      mma_commit(bar(L::QD_EMPTY + st));
+      mma_tn<DH, true>(tDV, tDP, do_mn0 + sd * kDStageLo, u > 0);
+      mma_commit(bar(L::DO_EMPTY + sd));
+      mma_tn<DH, true>(tDK, tDP + 32, q_mn0 + sq * kQStageLo, u > 0);
+      mma_commit(bar(L::Q_EMPTY + sq));
       if (more) {
-        mma_nt<DH>(tDP, v_lo, do_lo0 + st1 * kStageLo);
+        const int sd1 = (g + 1) % L::ND;
+        if (!bwait(bar(L::DO_FULL + sd1), ((g + 1) / L::ND) & 1, abort_flag, a)) { ok = false; break; }
+        tc_fence_after();
+        mma_nt<DH>(tDP, v_lo, do_lo0 + sd1 * kDStageLo);
         mma_commit(bar(L::DP_FULL));
       }
     }
@@ -436,13 +457,13 @@ __device__ void dkdv_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
     KvCursor cur;
     cur.init(a, it);
     for (int u = 0; u < ns; ++u, ++g, cur.next()) {
-      const uint8_t* stage = smem + L::ST_OFF + (g % L::NS) * L::STAGE;
+      const uint8_t* stage = smem + L::DO_OFF + (g % L::ND) * L::DSTAGE;
       const float* nl2 = reinterpret_cast<const float*>(stage + L::NL2_IN);
       const float* dl = reinterpret_cast<const float*>(stage + L::DL_IN);
       const bool diag = a.causal && cur.j == it.t;
-      // the per-column arrays arrived by bulk copy: acquire them through the
-      // stage's own barrier (already complete once S^T of this step exists)
-      if (!bwait_warp(bar(L::QD_FULL + g % L::NS), (g / L::NS) & 1, abort_flag, a)) return;
+      // the per-column arrays arrived by bulk copy with the step's dout tile:
+      // acquire them through that stage's barrier
+      if (!bwait_warp(bar(L::DO_FULL + g % L::ND), (g / L::ND) & 1, abort_flag, a)) return;
       if (!bwait_warp(bar(L::S_FULL), g & 1, abort_flag, a)) return;
       tc_fence_after();
       uint32_t sa[32], sb[32];
@@ -760,9 +781,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do, const BwdArgs a) {
   using L = KvLayout<DH>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the layout has no room to round the base up: refuse (status word) and
+  // return before any barrier or tensor memory is touched if it is not aligned
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusLayout);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);

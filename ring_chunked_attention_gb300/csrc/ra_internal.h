@@ -61,6 +61,7 @@ struct BwdArgs {
 
 // status word bits
 constexpr unsigned int kStatusTimeout = 1u;
+constexpr unsigned int kStatusLayout = 2u;  // a kernel found its shared memory base misaligned
 
 // ra_fwd.cu
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
