@@ -190,14 +190,19 @@ __device__ __forceinline__ int last_tile(const FwdArgs& a, const Item& it) {
   return j * a.tpc + a.tpc - 1;
 }
 
+// Query tile qt has allowed keys in key tile kt.
+__device__ __forceinline__ bool needs_tile(const FwdArgs& a, int qt, int kt) {
+  return !a.causal || a.k_tile0 + kt <= a.q_tile0 + qt;
+}
+
 __device__ __forceinline__ bool needs(const FwdArgs& a, const Item& it, int slot, int kt) {
   if (slot == 1 && !it.valid1) return false;
-  return !a.causal || a.k_tile0 + kt <= a.q_tile0 + it.qt[slot];
+  return needs_tile(a, slot ? it.qt[1] : it.qt[0], kt);
 }
 
 // The key tile is the query tile's diagonal (causal only): mask keys past the row.
-__device__ __forceinline__ bool is_diag(const FwdArgs& a, const Item& it, int slot, int kt) {
-  return a.causal && a.k_tile0 + kt == a.q_tile0 + it.qt[slot];
+__device__ __forceinline__ bool is_diag(const FwdArgs& a, int qt, int kt) {
+  return a.causal && a.k_tile0 + kt == a.q_tile0 + qt;
 }
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
@@ -483,9 +488,60 @@ struct RowState {
 };
 
 // One S tile of one slot: max, optional O rescale, exp, P -> TMEM.
+// Rescale this row's O accumulator by alpha (warp-uniform call: the TMEM
+// loads and stores are warp-collective; rows with alpha == 1 rewrite O unchanged).
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t o[32];
+    tmem_ld32(tO + c0, o);
+    tmem_wait_ld_regs(o);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+    tmem_st32(tO + c0, o);
+  }
+}
+
+// exp2 pass over the loaded row against reference m: bf16 P to TMEM over the
+// consumed S columns; returns the tile's exact sum and the sum of the rounded
+// weights (kRoundedSum).
+template <int D, bool DIAG>
+__device__ __forceinline__ void exp_pass(uint32_t tS, const uint32_t (&va)[32],
+                                         const uint32_t (&vb)[32], const uint32_t (&vc)[32],
+                                         const uint32_t (&vd)[32], int r, float c, float m,
+                                         float& sum_exact, float& sum_round) {
+  constexpr bool kRounded = !SoftmaxPolicy<D>::kExactMax;
+  const uint64_t c2 = f2_pack(c, c);
+  const uint64_t negm2 = f2_pack(-m, -m);
+  uint64_t se0 = 0, se1 = 0, sr0 = 0, sr1 = 0;
+  uint32_t pk[16];
+  chunk_exp<DIAG, kRounded>(va, 0, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  tmem_st16(tS + 0, pk);
+  chunk_exp<DIAG, kRounded>(vb, 32, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  tmem_st16(tS + 16, pk);
+  chunk_exp<DIAG, kRounded>(vc, 64, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  tmem_st16(tS + 32, pk);
+  chunk_exp<DIAG, kRounded>(vd, 96, r, c2, negm2, se0, se1, sr0, sr1, pk);
+  tmem_st16(tS + 48, pk);
+  const uint64_t se = f2_add(se0, se1), sr = f2_add(sr0, sr1);
+  sum_exact = f2_lo(se) + f2_hi(se);
+  sum_round = f2_lo(sr) + f2_hi(sr);
+}
+
+// One S tile of one slot: max, optional O rescale, exp, P -> TMEM.
+//
+// With the stale-reference policy (D = 128) a tile after the row's first
+// skips the max pass: the exps run against the current reference m, and the
+// tile's exact sum tells whether any weight grew large (a tile sum <= 2^30
+// bounds every weight by 2^30: representable in bf16, and O and l stay far
+// from fp32 overflow; the result is exact for any m since l and O share it).  Only when some row of the warp exceeds
+// that does the warp take the exact path: row max, new reference where the
+// max passed m + threshold, O rescale, exps again.
 template <int D, bool DIAG>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, float c, bool first,
                                              RowState& st) {
+  constexpr float kSpecLimit = 1073741824.0f;  // 2^30
   // the whole score row is loaded once (four 32-column loads in flight) and
   // stays in registers for both passes
   uint32_t va[32], vb[32], vc[32], vd[32];
@@ -497,53 +553,38 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, fl
   tmem_wait_ld_regs(vb);
   tmem_wait_ld_regs(vc);
   tmem_wait_ld_regs(vd);
-  // pass 1: row max
-  float mx = chunk_max<DIAG>(va, 0, r, -INFINITY);
-  mx = chunk_max<DIAG>(vb, 32, r, mx);
-  mx = chunk_max<DIAG>(vc, 64, r, mx);
-  mx = chunk_max<DIAG>(vd, 96, r, mx);
-  mx *= c;
-
-  // reference-max update; O is rescaled only when the max grows past the
-  // threshold (exact either way: l and O always share the same m)
-  float alpha = 1.0f;
-  if (first) {
-    st.m = mx;
-  } else if (mx > st.m + SoftmaxPolicy<D>::kRescaleThreshold) {
-    alpha = ex2(st.m - mx);
-    st.m = mx;
-    st.l_exact *= alpha;
-    st.l_round *= alpha;
+  float se, sr;
+  bool done = false;
+  if (!SoftmaxPolicy<D>::kExactMax && !first) {
+    exp_pass<D, DIAG>(tS, va, vb, vc, vd, r, c, st.m, se, sr);
+    done = !__any_sync(0xffffffffu, !(se <= kSpecLimit));  // also catches inf
+    if (!done) tmem_wait_st();  // the exact path rewrites the same columns
   }
-  if (!first && __any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t o[32];
-      tmem_ld32(tO + c0, o);
-      tmem_wait_ld_regs(o);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-      tmem_st32(tO + c0, o);
+  if (!done) {
+    // pass 1: row max
+    float mx = chunk_max<DIAG>(va, 0, r, -INFINITY);
+    mx = chunk_max<DIAG>(vb, 32, r, mx);
+    mx = chunk_max<DIAG>(vc, 64, r, mx);
+    mx = chunk_max<DIAG>(vd, 96, r, mx);
+    mx *= c;
+    // reference-max update; O is rescaled only when the max grows past the
+    // threshold (exact either way: l and O always share the same m)
+    float alpha = 1.0f;
+    if (first) {
+      st.m = mx;
+    } else if (mx > st.m + SoftmaxPolicy<D>::kRescaleThreshold) {
+      alpha = ex2(st.m - mx);
+      st.m = mx;
+      st.l_exact *= alpha;
+      st.l_round *= alpha;
     }
+    if (!first && __any_sync(0xffffffffu, alpha != 1.0f)) rescale_o<D>(tO, alpha);
+    // pass 2: exp2, sums, bf16 P written over the consumed S columns
+    exp_pass<D, DIAG>(tS, va, vb, vc, vd, r, c, st.m, se, sr);
   }
-
-  // pass 2: exp2, sums, bf16 P written over the consumed S columns
-  const uint64_t c2 = f2_pack(c, c);
-  const uint64_t negm2 = f2_pack(-st.m, -st.m);
-  uint64_t se0 = 0, se1 = 0, sr0 = 0, sr1 = 0;
-  uint32_t pk[16];
-  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(va, 0, r, c2, negm2, se0, se1, sr0, sr1, pk);
-  tmem_st16(tS + 0, pk);
-  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(vb, 32, r, c2, negm2, se0, se1, sr0, sr1, pk);
-  tmem_st16(tS + 16, pk);
-  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(vc, 64, r, c2, negm2, se0, se1, sr0, sr1, pk);
-  tmem_st16(tS + 32, pk);
-  chunk_exp<DIAG, !SoftmaxPolicy<D>::kExactMax>(vd, 96, r, c2, negm2, se0, se1, sr0, sr1, pk);
-  tmem_st16(tS + 48, pk);
-  const uint64_t se = f2_add(se0, se1), sr = f2_add(sr0, sr1);
-  st.l_exact += f2_lo(se) + f2_hi(se);
+  st.l_exact += se;
   if (SoftmaxPolicy<D>::kExactMax) st.l_round = st.l_exact;  // dominant weight is exactly 1
-  else st.l_round += f2_lo(sr) + f2_hi(sr);
+  else st.l_round += sr;
   tmem_wait_st();
 }
 
@@ -567,21 +608,25 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     if (x >= a.n_items) continue;
     const Item it = decode_item(a, x);
     if (slot == 1 && !it.valid1) continue;
+    // this slot's query tile and head, selected once: indexing the item with
+    // the run-time slot would place it in local memory
+    const int my_qt = slot ? it.qt[1] : it.qt[0];
+    const int my_h = slot ? it.h[1] : it.h[0];
     const int ns = n_steps(a, it);
-    if (ns == 0 || !needs(a, it, slot, 0)) {
+    if (ns == 0 || !needs_tile(a, my_qt, 0)) {
       // block mode only: no key of the block is allowed for these rows
-      const int srow = it.qt[slot] * kBM + r;
+      const int srow = my_qt * kBM + r;
       uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
-                                             (((size_t)it.b * a.S + srow) * a.H + it.h[slot]) * D);
+                                             (((size_t)it.b * a.S + srow) * a.H + my_h) * D);
 #pragma unroll 1
       for (int j = 0; j < D / 8; ++j) orow[j] = make_uint4(0, 0, 0, 0);
-      if (a.lse) a.lse[((size_t)it.b * a.H + it.h[slot]) * a.S + srow] = -INFINITY;
+      if (a.lse) a.lse[((size_t)it.b * a.H + my_h) * a.S + srow] = -INFINITY;
       continue;
     }
     // the slot's last step: the item's last one, or the one before it when
     // the slot does not need the last key tile (the second tile of a causal
     // pair in a one-chunk item)
-    const int u_last = (ns > 1 && !needs(a, it, slot, last_tile(a, it))) ? ns - 2 : ns - 1;
+    const int u_last = (ns > 1 && !needs_tile(a, my_qt, last_tile(a, it))) ? ns - 2 : ns - 1;
     StepCursor cur;
     cur.init(a, it);
 
@@ -589,10 +634,10 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     bool first = true;
     for (int u = 0; u < ns; ++u, cur.next()) {
       const int kt = cur.kt;
-      if (!needs(a, it, slot, kt)) continue;
+      if (!needs_tile(a, my_qt, kt)) continue;
       if (!wait_warp(bar(L::S_FULL + slot), n & 1, abort_flag, a)) return;
       tc_fence_after();
-      if (is_diag(a, it, slot, kt))
+      if (is_diag(a, my_qt, kt))
         softmax_tile<D, true>(tS, tO, r, c, first, st);
       else
         softmax_tile<D, false>(tS, tO, r, c, first, st);
@@ -606,8 +651,8 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         // epilogue: wait for the last O_i += P_i V, then out = O / l, lse
         if (!wait_warp(bar(L::O_FREE + slot), (n - 1) & 1, abort_flag, a)) return;
         tc_fence_after();
-        const int srow = it.qt[slot] * kBM + r;
-        const int h = it.h[slot];
+        const int srow = my_qt * kBM + r;
+        const int h = my_h;
         const float inv_l = 1.0f / st.l_round;
         uint4* orow = reinterpret_cast<uint4*>(
             static_cast<__nv_bfloat16*>(a.out) + (((size_t)it.b * a.S + srow) * a.H + h) * D);
