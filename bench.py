@@ -153,6 +153,26 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of ``values`` over every rank of the default
+    process group (the slowest rank decides a step's time); identity when no
+    group is initialised."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def weak_scaling_value(world_size: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time, in units of 1e12 per second."""
+    return world_size * units_per_rank / seconds / 1e12
+
+
 # ------------------------------------------------------------- CPU oracle arm
 def cpu_oracle_sample(w, budget_s: float = 15.0, seed: int = 0, inputs=None, full: bool = False):
     """Time the fp64 oracle (as it stands) on a bounded deterministic row
@@ -411,16 +431,11 @@ def run_ours(args):
     bwd = None if args.no_bwd else measure_bwd(ra, w, flush, stream, qd, kd, vd, out, lse)
 
     # slowest rank decides
-    if ws > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], device="cuda")
 
     flops = w.flops
-    value = ws * flops / (ms * 1e-3) / 1e12
-    e2e_value = ws * flops / (e2e_ms * 1e-3) / 1e12
+    value = weak_scaling_value(ws, flops, ms * 1e-3)
+    e2e_value = weak_scaling_value(ws, flops, e2e_ms * 1e-3)
     per_launch_tflops = flops / (ms * 1e-3) / 1e12
     peaks, src = load_peaks()
     peak = float(peaks["bf16_tflops"])

@@ -213,8 +213,10 @@ int ra_version(void);
  * Test hook for the failure path: when `timeout_ns` > 0, subsequent ra_fwd
  * and ra_bwd launches on this process use that wait limit instead of the default (2 s);
  * when `skip_value_load` != 0 the producer deliberately never issues the
- * first value-tile copy, so the consumer's bounded wait must run out and the
- * launch must report RA_ERR_TIMEOUT.  Pass (0, 0) to restore normal launches.
+ * first value-tile copy (ra_fwd) or the first output-gradient tile copy of
+ * the dk/dv kernel (ra_bwd, ra_bwd_static), so the consumer's bounded wait must
+ * run out and the launch must report RA_ERR_TIMEOUT.  Pass (0, 0) to restore
+ * normal launches.
  */
 void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
 

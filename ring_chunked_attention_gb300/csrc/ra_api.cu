@@ -342,6 +342,7 @@ ra_status launch_backward(DeviceInfo* dev, const void* q, const void* k, const v
   {
     std::lock_guard<std::mutex> lock(g_mu);
     a.timeout_ns = g_timeout_ns;
+    a.skip_first_load = g_skip_value_load;
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long units = (long long)B * S * H * (D / 8);

@@ -314,7 +314,8 @@ __device__ void dkdv_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
   const uint64_t pol_keep = l2_policy_evict_last();
   const uint64_t pol_once = l2_policy_evict_first();
   const int G = a.H / a.Hkv;
-  uint32_t kv_cnt = 0, g = 0;
+  uint32_t kv_cnt = 0, g = 0;  // g: steps whose q and dout copies were both issued
+  uint32_t q_cnt = 0;          // q copies issued (g or g + 1)
   bool ok = true;
   for (int k = 0; ok; ++k) {
     if (k * (int)gridDim.x >= a.n_items) break;
@@ -341,12 +342,14 @@ __device__ void dkdv_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
       for (int kb = 0; kb < L::DK; ++kb)
         tma_load_3d(sbase + L::Q_OFF + sq * L::TILE + kb * kBlk, tq, bar(L::Q_FULL + sq), kb * 64,
                     h, qrow, pol_keep);
+      ++q_cnt;
       if (!bwait(bar(L::DO_EMPTY + sd), ((g / L::ND) & 1) ^ 1, abort_flag, a)) { ok = false; break; }
       const uint32_t stage = sbase + L::DO_OFF + sd * L::DSTAGE;
       const uint32_t fb = bar(L::DO_FULL + sd);
       mbar_arrive_expect_tx(fb, L::TILE + 1024);
-      for (int kb = 0; kb < L::DK; ++kb)
-        tma_load_3d(stage + kb * kBlk, tdo, fb, kb * 64, h, qrow, pol_keep);
+      if (!(a.skip_first_load && g == 0))  // test hook: the stage then never completes
+        for (int kb = 0; kb < L::DK; ++kb)
+          tma_load_3d(stage + kb * kBlk, tdo, fb, kb * 64, h, qrow, pol_keep);
       const size_t li = ((size_t)it.b * a.H + h) * a.S + (size_t)cur.j * kT;
       bulk_load(stage + L::NL2_IN, a.nlse2 + li, 512, fb);
       bulk_load(stage + L::DL_IN, a.ndelta + li, 512, fb);
@@ -354,7 +357,8 @@ __device__ void dkdv_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
   }
   if (!ok) {  // let the copies in flight land before shared memory goes away
     if (kv_cnt > 0) wait_drain(bar(L::KV_FULL), (kv_cnt - 1) & 1, a.timeout_ns);
-    for (uint32_t c = (g > (uint32_t)L::NQ ? g - L::NQ : 0); c < g; ++c)
+    // every issued copy, including a q copy whose dout partner was never issued
+    for (uint32_t c = (q_cnt > (uint32_t)L::NQ ? q_cnt - L::NQ : 0); c < q_cnt; ++c)
       wait_drain(bar(L::Q_FULL + c % L::NQ), (c / L::NQ) & 1, a.timeout_ns);
     for (uint32_t c = (g > (uint32_t)L::ND ? g - L::ND : 0); c < g; ++c)
       wait_drain(bar(L::DO_FULL + c % L::ND), (c / L::ND) & 1, a.timeout_ns);
@@ -585,7 +589,8 @@ __device__ void dq_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
   auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
   const uint64_t pol_kv = l2_policy_evict_last();
   const uint64_t pol_q = l2_policy_evict_first();
-  uint32_t qd_cnt = 0, kv_cnt = 0;
+  uint32_t qd_cnt = 0, kv_cnt = 0;  // kv_cnt: steps whose K and V copies were both issued
+  uint32_t k_cnt = 0;               // K copies issued (kv_cnt or kv_cnt + 1)
   bool ok = true;
   for (int k = 0; ok; ++k) {
     if (k * (int)gridDim.x >= a.n_items) break;
@@ -611,6 +616,7 @@ __device__ void dq_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
       for (int kb = 0; kb < L::DK; ++kb)
         tma_load_3d(sbase + L::K_OFF + sk * L::TILE + kb * kBlk, tk, bar(L::K_FULL + sk), kb * 64,
                     it.kvh, row, pol_kv);
+      ++k_cnt;
       if (!bwait(bar(L::V_EMPTY + sv), ((kv_cnt / L::NV) & 1) ^ 1, abort_flag, a)) { ok = false; break; }
       mbar_arrive_expect_tx(bar(L::V_FULL + sv), L::TILE);
       for (int kb = 0; kb < L::DK; ++kb)
@@ -620,7 +626,8 @@ __device__ void dq_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
   }
   if (!ok) {
     if (qd_cnt > 0) wait_drain(bar(L::QD_FULL), (qd_cnt - 1) & 1, a.timeout_ns);
-    for (uint32_t c = (kv_cnt > (uint32_t)L::NK ? kv_cnt - L::NK : 0); c < kv_cnt; ++c)
+    // every issued copy, including a K copy whose V partner was never issued
+    for (uint32_t c = (k_cnt > (uint32_t)L::NK ? k_cnt - L::NK : 0); c < k_cnt; ++c)
       wait_drain(bar(L::K_FULL + c % L::NK), (c / L::NK) & 1, a.timeout_ns);
     for (uint32_t c = (kv_cnt > (uint32_t)L::NV ? kv_cnt - L::NV : 0); c < kv_cnt; ++c)
       wait_drain(bar(L::V_FULL + c % L::NV), (c / L::NV) & 1, a.timeout_ns);

@@ -229,7 +229,8 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
   const uint64_t pol_kv = l2_policy_evict_last();
   const uint64_t pol_q = l2_policy_evict_first();
   uint32_t q_cnt[2] = {0, 0};
-  uint32_t kv_cnt = 0;
+  uint32_t kv_cnt = 0;  // steps whose K and V copies were both issued
+  uint32_t k_cnt = 0;   // K copies issued (kv_cnt or kv_cnt + 1)
   bool ok = true;
   for (int k = 0; ok; ++k) {
     if (k * (int)gridDim.x >= a.n_items) break;
@@ -264,6 +265,7 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
       for (int kb = 0; kb < L::DK; ++kb)
         tma_load_3d(sbase + L::K_OFF + st * L::TILE + kb * L::BLOCK, tk, bar(L::K_FULL + st),
                     kb * 64, it.kvh, row, pol_kv);
+      ++k_cnt;
       if (!wait_bounded(bar(L::V_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
       mbar_arrive_expect_tx(bar(L::V_FULL + st), L::TILE);
       if (!(a.skip_value_load && kv_cnt == 0))
@@ -278,10 +280,11 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
     // wait (bounded) for the last armed phase of each full barrier.
     for (int slot = 0; slot < 2; ++slot)
       if (q_cnt[slot] > 0) wait_drain(bar(L::Q_FULL + slot), (q_cnt[slot] - 1) & 1, a.timeout_ns);
-    for (uint32_t c = (kv_cnt > (uint32_t)L::NS ? kv_cnt - L::NS : 0); c < kv_cnt; ++c) {
+    // every issued copy, including a K copy whose V partner was never issued
+    for (uint32_t c = (k_cnt > (uint32_t)L::NS ? k_cnt - L::NS : 0); c < k_cnt; ++c)
       wait_drain(bar(L::K_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
+    for (uint32_t c = (kv_cnt > (uint32_t)L::NS ? kv_cnt - L::NS : 0); c < kv_cnt; ++c)
       wait_drain(bar(L::V_FULL + c % L::NS), (c / L::NS) & 1, a.timeout_ns);
-    }
   }
 }
 

@@ -57,6 +57,8 @@ struct BwdArgs {
   float scale;           // multiplies dq and dk
   float scale_log2;      // scale * log2(e)
   unsigned long long timeout_ns;
+  int skip_first_load;   // failure-path test hook: the dk/dv producer never issues
+                         // its first dout-tile copy
 };
 
 // status word bits

@@ -30,3 +30,33 @@ def test_timeout_is_reported_and_context_survives(ralib, cuda_ok, oracle_mod):
     assert_parity(compare(out, lse, o_ref, l_ref), "after fault")
     x = torch.ones(1024, device="cuda")
     assert float((x * 2).sum()) == 2048.0
+
+
+@pytest.mark.parametrize("entry", ["ra_bwd", "ra_bwd_static"])
+def test_backward_timeout_is_reported_and_context_survives(ralib, cuda_ok, entry):
+    """The dk/dv producer skips its first output-gradient tile copy: the MMA
+    thread's bounded wait runs out, RA_ERR_TIMEOUT is reported, and the next
+    normal call reproduces the result of a call made before the fault."""
+    w = Workload("bfault", 1, 4, 2, 512, 128, 2, True)
+    q, k, v = (t.cuda() for t in make_inputs(w, seed=43))
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(44)).bfloat16().cuda()
+    out, lse = ralib.ra_fwd(q, k, v, P=w.P, causal=True)
+
+    def call():
+        if entry == "ra_bwd":
+            return ralib.ra_bwd(q, k, v, out, lse, do, P=w.P, causal=True)
+        bufs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        return ralib.ra_bwd_static(q, k, v, out, lse, do, *bufs, P=w.P, causal=True)
+
+    ref = call()
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK
+    ralib.ra_debug_set_fault(50_000_000, True)
+    try:
+        call()
+        assert ralib.ra_get_last_device_status() == ralib.RA_ERR_TIMEOUT
+    finally:
+        ralib.ra_debug_set_fault(0, False)
+    got = call()
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
