@@ -54,18 +54,22 @@ constexpr int kWarpMma = 9;
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr uint32_t kTmemCols = 512;
-// Reference-max policy of the online softmax, per head dimension.
-//  D = 128 (tensor-bound): the reference max m is refreshed only when a row's
-//    max grows by more than 2^8 (O is rescaled rarely); the dominant weight is
-//    then 2^(x - m) != 1 and its bf16 rounding would bias O / l, so the row
-//    keeps a second sum of the rounded weights for the output normalisation.
-//  D = 64 (softmax-bound): m always follows the exact running max, so the
-//    dominant weight is exactly 1 and one exact sum normalises both O and lse;
-//    the extra O rescales cost less than the second sum (measured).
+// Reference-max policy of the online softmax.  The reference max m is
+// refreshed only when a row's max grows by more than 2^8 (O is rescaled
+// rarely), and on tiles after a row's first the max pass is skipped unless a
+// weight grows past 2^30.  The dominant weight is then 2^(x - m) != 1, and its
+// bf16 rounding would bias O / l, so O is normalised by the sum of the
+// bf16-rounded weights, the ones the PV MMA used:
+//  D = 128: the softmax adds them up (a second sum beside the exact one);
+//  D = 64:  the PV MMA adds them up: it runs with N = D + 16 against a block of
+//    ones in shared memory, so O's column D holds the row sum of P in fp32.
+//    The extra columns cost no MMA time (an N = 64 MMA is bound by its issue
+//    cost, not its execution) and fit in tensor memory.
 template <int D>
 struct SoftmaxPolicy {
-  static constexpr bool kExactMax = (D == 64);
-  static constexpr float kRescaleThreshold = kExactMax ? 0.0f : 8.0f;  // log2 units
+  static constexpr bool kExactMax = false;
+  static constexpr float kRescaleThreshold = 8.0f;  // log2 units
+  static constexpr bool kMmaRowSum = (D == 64);
 };
 
 template <int D>
@@ -77,7 +81,11 @@ struct Layout {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
   static constexpr int V_OFF = K_OFF + NS * TILE;
-  static constexpr int BAR_OFF = V_OFF + NS * TILE;
+  // row-sum columns of the PV MMA (D = 64): one 64-column block of bf16 ones
+  static constexpr bool kRowSum = SoftmaxPolicy<D>::kMmaRowSum;
+  static constexpr int ONES_OFF = V_OFF + NS * TILE;
+  static constexpr int OW = kRowSum ? D + 16 : D;  // O columns per slot
+  static constexpr int BAR_OFF = ONES_OFF + (kRowSum ? BLOCK : 0);
   // barrier indices
   static constexpr int Q_FULL = 0, Q_EMPTY = 2, K_FULL = 4, K_EMPTY = 4 + NS, V_FULL = 4 + 2 * NS,
                        V_EMPTY = 4 + 3 * NS, S_FULL = 4 + 4 * NS, P_FULL = 6 + 4 * NS,
@@ -86,7 +94,7 @@ struct Layout {
   static constexpr int BYTES = MISC_OFF + 16;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
   __host__ __device__ static constexpr uint32_t S_COL(int i) { return 128u * i; }
-  __host__ __device__ static constexpr uint32_t O_COL(int i) { return 256u + (uint32_t)D * i; }
+  __host__ __device__ static constexpr uint32_t O_COL(int i) { return 256u + (uint32_t)OW * i; }
 };
 
 struct Item {
@@ -316,7 +324,7 @@ __device__ __forceinline__ void issue_s(uint32_t tS, uint32_t q_lo, uint32_t k_l
 
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo, bool accumulate) {
-  constexpr uint32_t idesc_pv = make_idesc(kBM, D, 1);
+  constexpr uint32_t idesc_pv = make_idesc(kBM, Layout<D>::OW, 1);
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk)
     mma_ts_lh(tO, tP + kk * 8, v_lo + (uint32_t)(kk * (2048 >> 4)), kDescHiSw128, idesc_pv,
@@ -333,8 +341,14 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   const uint32_t q_lo0 = desc_lo(sbase + L::Q_OFF, 16);
   const uint32_t q_lo1 = desc_lo(sbase + L::Q_OFF + L::TILE, 16);
   const uint32_t k_lo0 = desc_lo(sbase + L::K_OFF, 16);
-  const uint32_t v_lo0 = desc_lo(sbase + L::V_OFF, L::BLOCK);
+  const uint32_t v_lo0 = desc_lo(sbase + L::V_OFF, L::kRowSum ? (uint32_t)(L::ONES_OFF - L::V_OFF) : L::BLOCK);
   constexpr uint32_t kStageLo = (uint32_t)L::TILE >> 4;  // descriptor step between ring stages
+  // V of ring stage st: start address st tiles on; with the row-sum columns its
+  // second N block is the ones block, so the leading byte offset shrinks by a
+  // tile per stage (it lives in bits 16..29 of the descriptor's low word)
+  auto v_desc = [&](int st) -> uint32_t {
+    return L::kRowSum ? v_lo0 + st * kStageLo - ((st * kStageLo) << 16) : v_lo0 + st * kStageLo;
+  };
   uint32_t s_cnt0 = 0, s_cnt1 = 0;  // S MMAs issued per slot (== PV MMAs once a step is done)
   uint32_t q_cnt0 = 0, q_cnt1 = 0;
   uint32_t c = 0;                   // ring position of the current step
@@ -394,7 +408,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (n0) {
         if (!wait_bounded(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
-        issue_pv<D>(tO0, tS0, v_lo0 + st * kStageLo, !first0);
+        issue_pv<D>(tO0, tS0, v_desc(st), !first0);
         mma_commit(bar(L::O_FREE + 0));
         first0 = false;
       }
@@ -410,7 +424,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (n1) {
         if (!wait_bounded(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
         tc_fence_after();
-        issue_pv<D>(tO1, tS1, v_lo0 + st * kStageLo, !first1);
+        issue_pv<D>(tO1, tS1, v_desc(st), !first1);
         mma_commit(bar(L::O_FREE + 1));
         first1 = false;
       }
@@ -504,6 +518,13 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
     for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
     tmem_st32(tO + c0, o);
   }
+  if (Layout<D>::kRowSum) {  // the row-sum columns scale with O
+    uint32_t o[16];
+    tmem_ld16_wait(tO + D, o);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+    tmem_st16(tO + D, o);
+  }
 }
 
 // exp2 pass over the loaded row against reference m: bf16 P to TMEM over the
@@ -514,7 +535,7 @@ __device__ __forceinline__ void exp_pass(uint32_t tS, const uint32_t (&va)[32],
                                          const uint32_t (&vb)[32], const uint32_t (&vc)[32],
                                          const uint32_t (&vd)[32], int r, float c, float m,
                                          float& sum_exact, float& sum_round) {
-  constexpr bool kRounded = !SoftmaxPolicy<D>::kExactMax;
+  constexpr bool kRounded = !SoftmaxPolicy<D>::kExactMax && !SoftmaxPolicy<D>::kMmaRowSum;
   const uint64_t c2 = f2_pack(c, c);
   const uint64_t negm2 = f2_pack(-m, -m);
   uint64_t se0 = 0, se1 = 0, sr0 = 0, sr1 = 0;
@@ -656,7 +677,13 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         tc_fence_after();
         const int srow = my_qt * kBM + r;
         const int h = my_h;
-        const float inv_l = 1.0f / st.l_round;
+        float l_norm = st.l_round;
+        if (Layout<D>::kRowSum) {  // the PV MMA's row sum of the rounded weights
+          uint32_t ls[16];
+          tmem_ld16_wait(tO + D, ls);
+          l_norm = __uint_as_float(ls[0]);
+        }
+        const float inv_l = 1.0f / l_norm;
         uint4* orow = reinterpret_cast<uint4*>(
             static_cast<__nv_bfloat16*>(a.out) + (((size_t)it.b * a.S + srow) * a.H + h) * D);
 #pragma unroll 1
@@ -712,6 +739,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
+  }
+  if (L::kRowSum) {  // the B operand block of the row-sum columns: bf16 ones
+    uint4* ones = reinterpret_cast<uint4*>(smem + L::ONES_OFF);
+    for (int i = threadIdx.x; i < L::BLOCK / 16; i += kThreads)
+      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();  // visible to the tensor cores
   }
   tc_fence_before();
   __syncthreads();
