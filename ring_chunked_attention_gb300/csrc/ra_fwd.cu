@@ -26,7 +26,8 @@
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [  0,128) S_0   (P_0 as packed bf16 overwrites its first 64 columns)
 //   [128,256) S_1   (P_1 likewise)
-//   [256,256+D) O_0,  [256+D,256+2D) O_1
+//   [256,256+W) O_0,  [256+W,256+2W) O_1   with W = D = 128, or W = 80 at
+//   D = 64 (columns 64..79 hold the PV MMA's row sum of P)
 //
 // Every wait is bounded: on timeout the CTA raises a shared abort flag, sets
 // the device status word, lets its in-flight copies and MMAs finish (bounded
@@ -67,7 +68,6 @@ constexpr uint32_t kTmemCols = 512;
 //    cost, not its execution) and fit in tensor memory.
 template <int D>
 struct SoftmaxPolicy {
-  static constexpr bool kExactMax = false;
   static constexpr float kRescaleThreshold = 8.0f;  // log2 units
   static constexpr bool kMmaRowSum = (D == 64);
 };
@@ -504,7 +504,6 @@ struct RowState {
   float l_round;  // sum of the bf16-rounded exp2(x - m)
 };
 
-// One S tile of one slot: max, optional O rescale, exp, P -> TMEM.
 // Rescale this row's O accumulator by alpha (warp-uniform call: the TMEM
 // loads and stores are warp-collective; rows with alpha == 1 rewrite O unchanged).
 template <int D>
@@ -528,14 +527,14 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
 }
 
 // exp2 pass over the loaded row against reference m: bf16 P to TMEM over the
-// consumed S columns; returns the tile's exact sum and the sum of the rounded
-// weights (kRoundedSum).
+// consumed S columns; returns the tile's exact sum and, unless the PV MMA sums
+// the rounded weights itself (D = 64), their sum.
 template <int D, bool DIAG>
 __device__ __forceinline__ void exp_pass(uint32_t tS, const uint32_t (&va)[32],
                                          const uint32_t (&vb)[32], const uint32_t (&vc)[32],
                                          const uint32_t (&vd)[32], int r, float c, float m,
                                          float& sum_exact, float& sum_round) {
-  constexpr bool kRounded = !SoftmaxPolicy<D>::kExactMax && !SoftmaxPolicy<D>::kMmaRowSum;
+  constexpr bool kRounded = !SoftmaxPolicy<D>::kMmaRowSum;
   const uint64_t c2 = f2_pack(c, c);
   const uint64_t negm2 = f2_pack(-m, -m);
   uint64_t se0 = 0, se1 = 0, sr0 = 0, sr1 = 0;
@@ -555,13 +554,13 @@ __device__ __forceinline__ void exp_pass(uint32_t tS, const uint32_t (&va)[32],
 
 // One S tile of one slot: max, optional O rescale, exp, P -> TMEM.
 //
-// With the stale-reference policy (D = 128) a tile after the row's first
-// skips the max pass: the exps run against the current reference m, and the
-// tile's exact sum tells whether any weight grew large (a tile sum <= 2^30
-// bounds every weight by 2^30: representable in bf16, and O and l stay far
-// from fp32 overflow; the result is exact for any m since l and O share it).  Only when some row of the warp exceeds
-// that does the warp take the exact path: row max, new reference where the
-// max passed m + threshold, O rescale, exps again.
+// A tile after the row's first skips the max pass: the exps run against the
+// current reference m, and the tile's exact sum tells whether any weight grew
+// large (a tile sum <= 2^30 bounds every weight by 2^30: representable in
+// bf16, and O and l stay far from fp32 overflow; the result is exact for any
+// m since l and O share it).  Only when some row of the warp exceeds that does
+// the warp take the exact path: row max, new reference where the max passed
+// m + threshold, O rescale, exps again.
 template <int D, bool DIAG>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, float c, bool first,
                                              RowState& st) {
@@ -579,7 +578,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, fl
   tmem_wait_ld_regs(vd);
   float se, sr;
   bool done = false;
-  if (!SoftmaxPolicy<D>::kExactMax && !first) {
+  if (!first) {
     exp_pass<D, DIAG>(tS, va, vb, vc, vd, r, c, st.m, se, sr);
     done = !__any_sync(0xffffffffu, !(se <= kSpecLimit));  // also catches inf
     if (!done) tmem_wait_st();  // the exact path rewrites the same columns
@@ -607,8 +606,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, fl
     exp_pass<D, DIAG>(tS, va, vb, vc, vd, r, c, st.m, se, sr);
   }
   st.l_exact += se;
-  if (SoftmaxPolicy<D>::kExactMax) st.l_round = st.l_exact;  // dominant weight is exactly 1
-  else st.l_round += sr;
+  if (!SoftmaxPolicy<D>::kMmaRowSum) st.l_round += sr;  // else the PV MMA sums them
   tmem_wait_st();
 }
 
