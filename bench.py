@@ -43,15 +43,30 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["ring_chunked_attention_gb300/csrc/ra_fwd.cu",
                   "ring_chunked_attention_gb300/csrc/ra_ptx.cuh",
+                  "ring_chunked_attention_gb300/csrc/ra_umma.cuh",
+                  "ring_chunked_attention_gb300/csrc/ra_internal.h",
                   "ring_chunked_attention_gb300/csrc/ra_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with whitespace collapsed, so that a
+    comment-only edit does not count as a kernel change (string literals in
+    these files hold no comment markers)."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_sha() -> str:
+    """Hash of the code (comments and layout ignored) of the files that make up
+    the forward kernel and its launch."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
