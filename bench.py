@@ -357,6 +357,62 @@ def measure_bwd(ra, w, flush, stream, qd, kd, vd, out, lse, steps: int = 10):
             "peak_source": f"{src} bf16 dense burst"}
 
 
+def measure_e2e(ra, w, q, k, v, flush, steps: int):
+    """End to end through ra_fwd with the inputs in pinned host memory: every
+    step copies its q, k, v host -> device, runs the forward and reads out and
+    lse back device -> host.  Steps are pipelined over two device buffer sets
+    and three streams (copy in, compute, copy out), with events for every
+    dependency: step i's inputs upload while step i-1 computes and step i-2's
+    results download.  Returns (ms per step over the whole run, host->device
+    bytes per step, device->host bytes per step, steps)."""
+    import torch
+
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    dev = []
+    for _ in range(2):
+        dq_, dk_, dv_ = (torch.empty(t.shape, dtype=t.dtype, device="cuda") for t in (q, k, v))
+        dev.append((dq_, dk_, dv_, torch.empty_like(dq_),
+                    torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")))
+    outh = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(2)]
+    lseh = [torch.empty((w.B, w.H, w.S), dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
+    d2h = outh[0].numel() * 2 + lseh[0].numel() * 4
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(steps)]
+    ev_comp = [torch.cuda.Event() for _ in range(steps)]
+    ev_out = [torch.cuda.Event() for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(s_in)
+    for i in range(steps):
+        bq, bk, bv, bo, bl = dev[i % 2]
+        if i >= 2:
+            s_in.wait_event(ev_comp[i - 2])  # the kernel of step i-2 is done with these inputs
+        with torch.cuda.stream(s_in):
+            bq.copy_(qh, non_blocking=True)
+            bk.copy_(kh, non_blocking=True)
+            bv.copy_(vh, non_blocking=True)
+        ev_in[i].record(s_in)
+        s_comp.wait_event(ev_in[i])
+        if i >= 2:
+            s_comp.wait_event(ev_out[i - 2])  # step i-2's results were read back
+        with torch.cuda.stream(s_comp):
+            flush.fill_(1.0)
+            ra.ra_fwd(bq, bk, bv, P=w.P, causal=w.causal, scale=w.scale, out=bo, lse=bl,
+                      stream=s_comp)
+        ev_comp[i].record(s_comp)
+        s_out.wait_event(ev_comp[i])
+        with torch.cuda.stream(s_out):
+            outh[i % 2].copy_(bo, non_blocking=True)
+            lseh[i % 2].copy_(bl, non_blocking=True)
+        ev_out[i].record(s_out)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    if ra.ra_get_last_device_status() != 0:
+        raise RuntimeError("device status reported a timeout in the end-to-end steps")
+    return t0.elapsed_time(t1) / steps, h2d, d2h, steps
+
+
 def run_ours(args):
     import torch
 
@@ -421,26 +477,7 @@ def run_ours(args):
     ms = statistics.mean(kernel_ms)
 
     # end to end through the public call with host buffers (pinned), copies timed
-    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    outh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    lseh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    h2d = qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2
-    d2h = outh.numel() * 2 + lseh.numel() * 4
-    e2e_steps = max(3, min(args.steps, 10))
-    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(e2e_steps + 1)]
-    for i, (e0, e1) in enumerate(e2e_evs):
-        flush.fill_(1.0)
-        e0.record(stream)
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        step()
-        outh.copy_(out, non_blocking=True)
-        lseh.copy_(lse, non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in e2e_evs[1:])
+    e2e_ms, h2d, d2h, e2e_steps = measure_e2e(ra, w, q, k, v, flush, max(10, min(args.steps, 30)))
 
     merge = None if args.no_merge else measure_merge(ra, w, flush, stream)
     bwd = None if args.no_bwd else measure_bwd(ra, w, flush, stream, qd, kd, vd, out, lse)
@@ -478,7 +515,10 @@ def run_ours(args):
                          "traffic": traffic},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
+                    "pipelining": "two device buffer sets, three streams: step i's inputs "
+                                  "upload while step i-1 computes and step i-2's out/lse "
+                                  "download; the time covers every copy of every step"},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms),

@@ -18,6 +18,7 @@ CASES = [
     ("straddling_block", 1, 2, 2, 384, 256, 128, 128, 256, True),
     ("noncausal_block", 1, 4, 4, 256, 640, 64, 0, 4096, False),
     ("single_tile_rows", 1, 3, 1, 128, 256, 128, 128, 0, True),
+    ("diag_block_d64_qtiles", 1, 3, 3, 256, 384, 64, 256, 128, True),
 ]
 
 

@@ -163,14 +163,19 @@ def test_lse_optional(ralib, cuda_ok):
     assert l2 is None and torch.equal(o1, o2)
 
 
-def test_peaked_softmax_rescaling(ralib, cuda_ok, oracle_mod):
-    # std 3 on q and k at D = 128: scores with std 9, max jumps by far more
-    # than the 2^8 rescale threshold inside a row
-    w = Workload("peak", 1, 2, 2, 1024, 128, 4, True, sigma_qk=3.0)
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("sigma", [3.0, 6.0])
+def test_peaked_softmax_rescaling(ralib, cuda_ok, oracle_mod, D, sigma):
+    """std sigma on q and k: scores with std sigma^2 (x sqrt(D) scale), so a
+    row's max jumps by far more than the 2^8 rescale threshold between tiles;
+    at sigma = 6 the jumps also pass the 2^30 guard of the skipped max pass,
+    so warps take the exact path (max pass, O rescale, which at D = 64 also
+    rescales the PV MMA's row-sum columns)."""
+    w = Workload("peak", 1, 2, 2, 1024, D, 4, True, sigma_qk=sigma)
     q, k, v = make_inputs(w, seed=23)
     out, lse = _run(ralib, q, k, v, w)
     o_ref, l_ref = oracle_mod.attn_direct(q, k, v, True, w.scale)
-    assert_parity(compare(out, lse, o_ref, l_ref), "peaked")
+    assert_parity(compare(out, lse, o_ref, l_ref), f"peaked D={D} sigma={sigma}")
 
 
 def test_stream_argument_is_used(ralib, cuda_ok, oracle_mod):
