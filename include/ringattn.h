@@ -235,6 +235,19 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
  */
 void ra_set_mma_order(int strict);
 
+/*
+ * How ra_fwd and ra_fwd_block group query tiles into work items (no
+ * counterpart on the pages; an implementation choice of this library).  A
+ * paired item is two 128-row query tiles that share one key/value stream (two
+ * heads of a GQA group, or two consecutive tiles of one head); a single item
+ * is one tile.  policy 0 (default): pair, unless that leaves fewer items than
+ * the device has SMs, when single items shorten the heaviest item; 1: pair
+ * whenever the shape allows; 2: never pair.  Results agree to rounding; the
+ * policy exists so that tests can reach every grouping at small sizes.
+ * Applies to launches made after the call.
+ */
+void ra_set_item_pairing(int policy);
+
 /* Drop cached tensor maps and device queries (no device memory is held). */
 void ra_shutdown(void);
 

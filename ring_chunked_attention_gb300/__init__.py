@@ -21,7 +21,8 @@ import ctypes
 import os
 
 __all__ = ["ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
-           "ra_debug_set_fault", "ra_set_mma_order", "ra_shutdown", "ra_version", "RaError", "library_path",
+           "ra_debug_set_fault", "ra_set_mma_order", "ra_set_item_pairing", "ra_shutdown", "ra_version",
+           "RaError", "library_path",
            "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT"]
 
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = 0, 1, 2, 3, 4
@@ -32,7 +33,7 @@ _lib = None
 
 EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
            "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_set_mma_order",
-           "ra_shutdown")
+           "ra_set_item_pairing", "ra_shutdown")
 
 
 class RaError(RuntimeError):
@@ -81,6 +82,8 @@ def _load():
     lib.ra_debug_set_fault.restype = None
     lib.ra_set_mma_order.argtypes = [i]
     lib.ra_set_mma_order.restype = None
+    lib.ra_set_item_pairing.argtypes = [i]
+    lib.ra_set_item_pairing.restype = None
     lib.ra_shutdown.argtypes = []
     lib.ra_shutdown.restype = None
     _lib = lib
@@ -297,6 +300,11 @@ def ra_set_mma_order(strict: bool) -> None:
     """Strict (wait for each PV before rewriting S) or default in-order MMA
     issue for subsequent ra_fwd launches; see include/ringattn.h."""
     _load().ra_set_mma_order(int(bool(strict)))
+
+
+def ra_set_item_pairing(policy: int) -> None:
+    """0 automatic (default), 1 pair query tiles whenever possible, 2 never."""
+    _load().ra_set_item_pairing(int(policy))
 
 
 def ra_shutdown() -> None:

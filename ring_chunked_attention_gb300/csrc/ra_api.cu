@@ -25,6 +25,7 @@ std::mutex g_mu;
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 int g_skip_value_load = 0;
 int g_strict_mma_order = 0;
+int g_item_pairing = 0;  // 0 automatic, 1 always pair when the shape allows, 2 never pair
 
 // per-device facts, queried once
 struct DeviceInfo {
@@ -198,11 +199,21 @@ ra_status launch_attention(const void* q, const void* k, const void* v, void* ou
   }
   a.n_items = a.groups * a.nq;
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  int pairing;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     a.timeout_ns = g_timeout_ns;
     a.skip_value_load = g_skip_value_load;
     a.strict_mma_order = g_strict_mma_order;
+    pairing = g_item_pairing;
+  }
+  // With fewer paired items than SMs the heaviest pair is the critical path:
+  // one query tile per item halves it and fills the SMs better.
+  if (a.mode != ra::MODE_SINGLE && (pairing == 2 || (pairing == 0 && a.n_items < dev->sms))) {
+    a.mode = ra::MODE_SINGLE;
+    a.groups = B * H;
+    a.nq = a.tiles;
+    a.n_items = a.groups * a.nq;
   }
   const int grid = a.n_items < dev->sms ? a.n_items : dev->sms;
   cudaError_t e = ra::launch_fwd(D, tq, tk, tv, a, grid, static_cast<cudaStream_t>(stream));
@@ -428,6 +439,11 @@ void ra_set_mma_order(int strict) {
   g_strict_mma_order = strict ? 1 : 0;
 }
 
+void ra_set_item_pairing(int policy) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_item_pairing = (policy == 1 || policy == 2) ? policy : 0;
+}
+
 void ra_shutdown(void) {
   std::lock_guard<std::mutex> lock(g_mu);
   for (auto& e : g_maps) e.used = false;
@@ -435,6 +451,7 @@ void ra_shutdown(void) {
   g_timeout_ns = kDefaultTimeoutNs;
   g_skip_value_load = 0;
   g_strict_mma_order = 0;
+  g_item_pairing = 0;
 }
 
 }  // extern "C"

@@ -22,8 +22,16 @@ CASES = [
 ]
 
 
+@pytest.fixture(params=[0, 1], ids=["auto", "paired"])
+def pairing(request, ralib):
+    """Automatic work-item grouping and forced pairing of query tiles."""
+    ralib.ra_set_item_pairing(request.param)
+    yield request.param
+    ralib.ra_set_item_pairing(0)
+
+
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_block_parity(ralib, cuda_ok, oracle_mod, case):
+def test_block_parity(ralib, cuda_ok, oracle_mod, case, pairing):
     name, B, H, Hkv, Sq, Sk, D, qp, kp, causal = case
     g = torch.Generator().manual_seed(sum(case[1:8]))
     q = torch.randn(B, Sq, H, D, generator=g).bfloat16()

@@ -41,8 +41,18 @@ SMALL = [
 ]
 
 
+@pytest.fixture(params=[0, 1], ids=["auto", "paired"])
+def pairing(request, ralib):
+    """Work-item grouping: automatic (small launches use one query tile per
+    item) and forced pairing (two heads of a group, or two consecutive tiles),
+    so that every grouping is checked at sizes the oracle covers in full."""
+    ralib.ra_set_item_pairing(request.param)
+    yield request.param
+    ralib.ra_set_item_pairing(0)
+
+
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
-def test_small_parity_all_rows(ralib, cuda_ok, oracle_mod, case):
+def test_small_parity_all_rows(ralib, cuda_ok, oracle_mod, case, pairing):
     name, B, H, Hkv, S, D, P, causal = case
     w = Workload(name, B, H, Hkv, S, D, P, causal)
     q, k, v = make_inputs(w, seed=7)
@@ -200,6 +210,7 @@ def test_default_mma_order_is_bit_identical_to_strict_order(ralib, cuda_ok, name
     q, k, v = make_inputs(w, seed=43)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     outs = []
+    ralib.ra_set_item_pairing(1)  # the paired chains are the ones the order matters for
     try:
         for strict in (True, False, False):
             ralib.ra_set_mma_order(strict)
@@ -209,5 +220,6 @@ def test_default_mma_order_is_bit_identical_to_strict_order(ralib, cuda_ok, name
             outs.append((o, l))
     finally:
         ralib.ra_set_mma_order(False)
+        ralib.ra_set_item_pairing(0)
     for o, l in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
