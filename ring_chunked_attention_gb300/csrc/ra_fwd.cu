@@ -472,12 +472,13 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], int j0, int 
 }
 
 // p = exp2(x*c - m) for one 32-column chunk; packs bf16 pairs into pk and
-// accumulates both the exact fp32 sum (for lse) and the sum of the rounded
-// values that the PV product consumes (for the output normalisation).
-template <bool DIAG, bool kRoundedSum>
+// accumulates the exact fp32 sum (for lse).  The sum of the rounded values
+// that the PV product consumes (for the output normalisation) is taken later
+// from the packed pairs, off the path to the PV product.
+template <bool DIAG>
 __device__ __forceinline__ void chunk_exp(const uint32_t (&v)[32], int j0, int r, uint64_t c2,
                                           uint64_t negm2, uint64_t& se0, uint64_t& se1,
-                                          uint64_t& sr0, uint64_t& sr1, uint32_t (&pk)[16]) {
+                                          uint32_t (&pk)[16]) {
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
     const uint64_t xs = f2_fma(f2_pack(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), c2, negm2);
@@ -489,13 +490,33 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&v)[32], int j0, int r
     const uint32_t pr = pack_bf16x2(p0, p1);
     if ((j & 2) == 0) se0 = f2_add(se0, f2_pack(p0, p1));
     else se1 = f2_add(se1, f2_pack(p0, p1));
-    if (kRoundedSum) {
-      const uint64_t prf = ((uint64_t)(pr & 0xFFFF0000u) << 32) | (uint64_t)(pr << 16);
-      if ((j & 2) == 0) sr0 = f2_add(sr0, prf);
-      else sr1 = f2_add(sr1, prf);
-    }
     pk[j >> 1] = pr;
   }
+}
+
+struct PackedRow {  // a row's 128 bf16 weights in pairs, by 32-column chunk
+  uint32_t a[16], b[16], c[16], d[16];
+};
+
+__device__ __forceinline__ void rounded_sum_chunk(const uint32_t (&pk)[16], uint64_t& s0,
+                                                  uint64_t& s1) {
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    s0 = f2_add(s0, ((uint64_t)(pk[i] & 0xFFFF0000u) << 32) | (uint64_t)(pk[i] << 16));
+    s1 = f2_add(s1, ((uint64_t)(pk[i + 1] & 0xFFFF0000u) << 32) | (uint64_t)(pk[i + 1] << 16));
+  }
+}
+
+// fp32 sum of the row's bf16 weights: the normaliser of the output, which
+// accumulates exactly these rounded values
+__device__ __forceinline__ float rounded_sum(const PackedRow& pk) {
+  uint64_t s0 = 0, s1 = 0;
+  rounded_sum_chunk(pk.a, s0, s1);
+  rounded_sum_chunk(pk.b, s0, s1);
+  rounded_sum_chunk(pk.c, s0, s1);
+  rounded_sum_chunk(pk.d, s0, s1);
+  const uint64_t t = f2_add(s0, s1);
+  return f2_lo(t) + f2_hi(t);
 }
 
 struct RowState {
@@ -526,87 +547,103 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
   }
 }
 
-// exp2 pass over the loaded row against reference m: bf16 P to TMEM over the
-// consumed S columns; returns the tile's exact sum and, unless the PV MMA sums
-// the rounded weights itself (D = 64), their sum.
-template <int D, bool DIAG>
-__device__ __forceinline__ void exp_pass(uint32_t tS, const uint32_t (&va)[32],
-                                         const uint32_t (&vb)[32], const uint32_t (&vc)[32],
-                                         const uint32_t (&vd)[32], int r, float c, float m,
-                                         float& sum_exact, float& sum_round) {
-  constexpr bool kRounded = !SoftmaxPolicy<D>::kMmaRowSum;
+// exp2 of one score row against reference m, into registers: bf16 weights
+// packed in pairs and their exact fp32 sum (the scores stay in tensor memory).
+template <bool DIAG>
+__device__ __forceinline__ float exp_row(const uint32_t (&va)[32], const uint32_t (&vb)[32],
+                                         const uint32_t (&vc)[32], const uint32_t (&vd)[32], int r,
+                                         float c, float m, PackedRow& pk) {
   const uint64_t c2 = f2_pack(c, c);
   const uint64_t negm2 = f2_pack(-m, -m);
-  uint64_t se0 = 0, se1 = 0, sr0 = 0, sr1 = 0;
-  uint32_t pk[16];
-  chunk_exp<DIAG, kRounded>(va, 0, r, c2, negm2, se0, se1, sr0, sr1, pk);
-  tmem_st16(tS + 0, pk);
-  chunk_exp<DIAG, kRounded>(vb, 32, r, c2, negm2, se0, se1, sr0, sr1, pk);
-  tmem_st16(tS + 16, pk);
-  chunk_exp<DIAG, kRounded>(vc, 64, r, c2, negm2, se0, se1, sr0, sr1, pk);
-  tmem_st16(tS + 32, pk);
-  chunk_exp<DIAG, kRounded>(vd, 96, r, c2, negm2, se0, se1, sr0, sr1, pk);
-  tmem_st16(tS + 48, pk);
-  const uint64_t se = f2_add(se0, se1), sr = f2_add(sr0, sr1);
-  sum_exact = f2_lo(se) + f2_hi(se);
-  sum_round = f2_lo(sr) + f2_hi(sr);
+  uint64_t se0 = 0, se1 = 0;
+  chunk_exp<DIAG>(va, 0, r, c2, negm2, se0, se1, pk.a);
+  chunk_exp<DIAG>(vb, 32, r, c2, negm2, se0, se1, pk.b);
+  chunk_exp<DIAG>(vc, 64, r, c2, negm2, se0, se1, pk.c);
+  chunk_exp<DIAG>(vd, 96, r, c2, negm2, se0, se1, pk.d);
+  const uint64_t se = f2_add(se0, se1);
+  return f2_lo(se) + f2_hi(se);
 }
 
-// One S tile of one slot: max, optional O rescale, exp, P -> TMEM.
+template <bool DIAG>
+__device__ __forceinline__ float row_max(const uint32_t (&va)[32], const uint32_t (&vb)[32],
+                                         const uint32_t (&vc)[32], const uint32_t (&vd)[32], int r) {
+  float mx = chunk_max<DIAG>(va, 0, r, -INFINITY);
+  mx = chunk_max<DIAG>(vb, 32, r, mx);
+  mx = chunk_max<DIAG>(vc, 64, r, mx);
+  return chunk_max<DIAG>(vd, 96, r, mx);
+}
+
+// One S tile of one slot: bf16 P to tensor memory over the consumed S
+// columns, the tile's exact sum into l; the packed weights are returned so
+// that the caller can take their rounded sum once P has been handed over.
 //
-// A tile after the row's first skips the max pass: the exps run against the
-// current reference m, and the tile's exact sum tells whether any weight grew
-// large (a tile sum <= 2^30 bounds every weight by 2^30: representable in
-// bf16, and O and l stay far from fp32 overflow; the result is exact for any
-// m since l and O share it).  Only when some row of the warp exceeds that does
-// the warp take the exact path: row max, new reference where the max passed
-// m + threshold, O rescale, exps again.
+// The row's first tile sets the reference m to its max.  A later tile skips
+// the max pass: the exps run against the current m, and the tile's exact sum
+// tells whether any weight grew large (a tile sum <= 2^30 bounds every weight
+// by 2^30: representable in bf16, and O and l stay far from fp32 overflow;
+// the result is exact for any m since l and O share it).  Only when some row
+// of the warp exceeds that does the warp take the exact path, on the scores
+// read again from tensor memory (P is stored only once the weights are
+// accepted): row max, new reference where the max passed m + threshold, O
+// rescale, exps again.
 template <int D, bool DIAG>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, float c, bool first,
-                                             RowState& st) {
+                                             RowState& st, PackedRow& pk) {
   constexpr float kSpecLimit = 1073741824.0f;  // 2^30
-  // the whole score row is loaded once (four 32-column loads in flight) and
-  // stays in registers for both passes
-  uint32_t va[32], vb[32], vc[32], vd[32];
-  tmem_ld32(tS + 0, va);
-  tmem_ld32(tS + 32, vb);
-  tmem_ld32(tS + 64, vc);
-  tmem_ld32(tS + 96, vd);
-  tmem_wait_ld_regs(va);
-  tmem_wait_ld_regs(vb);
-  tmem_wait_ld_regs(vc);
-  tmem_wait_ld_regs(vd);
-  float se, sr;
-  bool done = false;
-  if (!first) {
-    exp_pass<D, DIAG>(tS, va, vb, vc, vd, r, c, st.m, se, sr);
-    done = !__any_sync(0xffffffffu, !(se <= kSpecLimit));  // also catches inf
-    if (!done) tmem_wait_st();  // the exact path rewrites the same columns
+  float se;
+  {
+    uint32_t va[32], vb[32], vc[32], vd[32];
+    tmem_ld32(tS + 0, va);
+    tmem_ld32(tS + 32, vb);
+    tmem_ld32(tS + 64, vc);
+    tmem_ld32(tS + 96, vd);
+    tmem_wait_ld_regs(va);
+    tmem_wait_ld_regs(vb);
+    tmem_wait_ld_regs(vc);
+    tmem_wait_ld_regs(vd);
+    if (first) st.m = row_max<DIAG>(va, vb, vc, vd, r) * c;
+    se = exp_row<DIAG>(va, vb, vc, vd, r, c, st.m, pk);
   }
-  if (!done) {
-    // pass 1: row max
-    float mx = chunk_max<DIAG>(va, 0, r, -INFINITY);
-    mx = chunk_max<DIAG>(vb, 32, r, mx);
-    mx = chunk_max<DIAG>(vc, 64, r, mx);
-    mx = chunk_max<DIAG>(vd, 96, r, mx);
+  // never taken on the first tile: its weights are at most 1
+  if (__any_sync(0xffffffffu, !(se <= kSpecLimit))) {  // also catches inf
+    // rare: stream the scores again from tensor memory, one chunk at a time
+    float mx = -INFINITY;
+    {
+      uint32_t w[32];
+      tmem_ld32(tS + 0, w); tmem_wait_ld_regs(w); mx = chunk_max<DIAG>(w, 0, r, mx);
+      tmem_ld32(tS + 32, w); tmem_wait_ld_regs(w); mx = chunk_max<DIAG>(w, 32, r, mx);
+      tmem_ld32(tS + 64, w); tmem_wait_ld_regs(w); mx = chunk_max<DIAG>(w, 64, r, mx);
+      tmem_ld32(tS + 96, w); tmem_wait_ld_regs(w); mx = chunk_max<DIAG>(w, 96, r, mx);
+    }
     mx *= c;
-    // reference-max update; O is rescaled only when the max grows past the
-    // threshold (exact either way: l and O always share the same m)
+    // O is rescaled only when the max grows past the threshold (exact either
+    // way: l and O always share the same m)
     float alpha = 1.0f;
-    if (first) {
-      st.m = mx;
-    } else if (mx > st.m + SoftmaxPolicy<D>::kRescaleThreshold) {
+    if (mx > st.m + SoftmaxPolicy<D>::kRescaleThreshold) {
       alpha = ex2(st.m - mx);
       st.m = mx;
       st.l_exact *= alpha;
       st.l_round *= alpha;
     }
-    if (!first && __any_sync(0xffffffffu, alpha != 1.0f)) rescale_o<D>(tO, alpha);
-    // pass 2: exp2, sums, bf16 P written over the consumed S columns
-    exp_pass<D, DIAG>(tS, va, vb, vc, vd, r, c, st.m, se, sr);
+    if (__any_sync(0xffffffffu, alpha != 1.0f)) rescale_o<D>(tO, alpha);
+    const uint64_t c2 = f2_pack(c, c);
+    const uint64_t negm2 = f2_pack(-st.m, -st.m);
+    uint64_t se0 = 0, se1 = 0;
+    {
+      uint32_t w[32];
+      tmem_ld32(tS + 0, w); tmem_wait_ld_regs(w); chunk_exp<DIAG>(w, 0, r, c2, negm2, se0, se1, pk.a);
+      tmem_ld32(tS + 32, w); tmem_wait_ld_regs(w); chunk_exp<DIAG>(w, 32, r, c2, negm2, se0, se1, pk.b);
+      tmem_ld32(tS + 64, w); tmem_wait_ld_regs(w); chunk_exp<DIAG>(w, 64, r, c2, negm2, se0, se1, pk.c);
+      tmem_ld32(tS + 96, w); tmem_wait_ld_regs(w); chunk_exp<DIAG>(w, 96, r, c2, negm2, se0, se1, pk.d);
+    }
+    const uint64_t sum = f2_add(se0, se1);
+    se = f2_lo(sum) + f2_hi(sum);
   }
+  tmem_st16(tS + 0, pk.a);
+  tmem_st16(tS + 16, pk.b);
+  tmem_st16(tS + 32, pk.c);
+  tmem_st16(tS + 48, pk.d);
   st.l_exact += se;
-  if (!SoftmaxPolicy<D>::kMmaRowSum) st.l_round += sr;  // else the PV MMA sums them
   tmem_wait_st();
 }
 
@@ -659,13 +696,18 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (!needs_tile(a, my_qt, kt)) continue;
       if (!wait_warp(bar(L::S_FULL + slot), n & 1, abort_flag, a)) return;
       tc_fence_after();
+      PackedRow pk;
       if (is_diag(a, my_qt, kt))
-        softmax_tile<D, true>(tS, tO, r, c, first, st);
+        softmax_tile<D, true>(tS, tO, r, c, first, st, pk);
       else
-        softmax_tile<D, false>(tS, tO, r, c, first, st);
+        softmax_tile<D, false>(tS, tO, r, c, first, st, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::P_FULL + slot));
+      // the sum of the rounded weights is needed only by the epilogue: taken
+      // here, while the tensor cores run this slot's PV and next S products
+      // (with the row-sum columns the PV product sums them itself)
+      if (!SoftmaxPolicy<D>::kMmaRowSum) st.l_round += rounded_sum(pk);
       ++n;
       first = false;
 
