@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "ra_internal.h"
@@ -203,11 +204,6 @@ __device__ __forceinline__ bool needs_tile(const FwdArgs& a, int qt, int kt) {
   return !a.causal || a.k_tile0 + kt <= a.q_tile0 + qt;
 }
 
-__device__ __forceinline__ bool needs(const FwdArgs& a, const Item& it, int slot, int kt) {
-  if (slot == 1 && !it.valid1) return false;
-  return needs_tile(a, slot ? it.qt[1] : it.qt[0], kt);
-}
-
 // The key tile is the query tile's diagonal (causal only): mask keys past the row.
 __device__ __forceinline__ bool is_diag(const FwdArgs& a, int qt, int kt) {
   return a.causal && a.k_tile0 + kt == a.q_tile0 + qt;
@@ -367,20 +363,24 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (!wait_bounded(bar(L::Q_FULL + 1), q_cnt1 & 1, abort_flag, a)) break;
       ++q_cnt1;
     }
+    // slot i needs key tile kt iff kt <= lim_i (needs_tile's causal test,
+    // taken once per item instead of per step; -1: the item has no slot 1)
+    const int lim0 = a.causal ? a.q_tile0 + it.qt[0] - a.k_tile0 : INT_MAX;
+    const int lim1 = !it.valid1 ? -1 : (a.causal ? a.q_tile0 + it.qt[1] - a.k_tile0 : INT_MAX);
     StepCursor nxt;  // the step whose S MMAs are issued next
     nxt.init(a, it);
     // prologue: S(0) for both slots
     {
       const int st = c % L::NS;
       if (!wait_bounded(bar(L::K_FULL + st), (c / L::NS) & 1, abort_flag, a)) break;
-      if (needs(a, it, 0, nxt.kt)) {
+      if (nxt.kt <= lim0) {
         if (s_cnt0 > 0 && !wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) break;
         tc_fence_after();
         issue_s<D>(tS0, q_lo0, k_lo0 + st * kStageLo);
         mma_commit(bar(L::S_FULL + 0));
         ++s_cnt0;
       }
-      if (needs(a, it, 1, nxt.kt)) {
+      if (nxt.kt <= lim1) {
         if (s_cnt1 > 0 && !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) break;
         tc_fence_after();
         issue_s<D>(tS1, q_lo1, k_lo0 + st * kStageLo);
@@ -396,10 +396,10 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     bool first0 = true, first1 = true;
     for (int u = 0; u < ns && ok; ++u, ++c) {
       const int st = c % L::NS;
-      const bool n0 = needs(a, it, 0, nxt.kt), n1 = needs(a, it, 1, nxt.kt);
+      const bool n0 = nxt.kt <= lim0, n1 = nxt.kt <= lim1;
       const bool more = u + 1 < ns;
       if (more) nxt.next();
-      const bool m0 = more && needs(a, it, 0, nxt.kt), m1 = more && needs(a, it, 1, nxt.kt);
+      const bool m0 = more && nxt.kt <= lim0, m1 = more && nxt.kt <= lim1;
       const int st1 = (c + 1) % L::NS;
       if (!wait_bounded(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
       if (more &&
