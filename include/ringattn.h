@@ -17,7 +17,14 @@
  *   - Every pointer to tensor data is a DEVICE pointer into memory the caller
  *     owns; the library never allocates, frees or retains caller memory.  The
  *     only library-owned device state is one status word per device (see
- *     ra_get_last_device_status) and the kernels' code.
+ *     ra_get_last_device_status), 64 work-item counters per device for the
+ *     forward kernel, the static scratch of ra_bwd_static, and the kernels' code.
+ *   - ra_fwd and ra_fwd_block hand out their work items at run time through a
+ *     counter that each launch takes in turn from the device's 64 and leaves at
+ *     zero when it ends: up to 64 of these launches may be in flight on one
+ *     device at once (on any streams).  A launch captured into a CUDA graph
+ *     keeps its counter, so one captured launch must not run concurrently
+ *     with itself (replays of it in one stream are fine).
  *   - Every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and returns without waiting; results are valid once the
  *     stream has reached the work.

@@ -34,6 +34,8 @@ struct DeviceInfo {
   int sms = 0;
   unsigned int* status = nullptr;
   float* bwd_scratch = nullptr;  // the static scratch of ra_bwd_static on this device
+  unsigned int* item_ctr = nullptr;  // the forward's work-item counter slots on this device
+  unsigned int launches = 0;         // forward launches so far (picks the counter slot)
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -55,10 +57,13 @@ ra_status device_info(DeviceInfo** out) {
     if ((e = ra::status_word_ptr(&st)) != cudaSuccess) return cuda_fail(e);
     float* scratch = nullptr;
     if ((e = ra::bwd_static_scratch(&scratch)) != cudaSuccess) return cuda_fail(e);
+    unsigned int* ctr = nullptr;
+    if ((e = ra::item_counter_ptr(&ctr)) != cudaSuccess) return cuda_fail(e);
     d.sm103 = (major == 10 && minor == 3);
     d.sms = sms;
     d.status = st;
     d.bwd_scratch = scratch;
+    d.item_ctr = ctr;
     d.valid = true;
   }
   *out = &d;
@@ -206,6 +211,8 @@ ra_status launch_attention(const void* q, const void* k, const void* v, void* ou
     a.skip_value_load = g_skip_value_load;
     a.strict_mma_order = g_strict_mma_order;
     pairing = g_item_pairing;
+    // each launch takes the next counter slot; the kernel leaves it at zero
+    a.item_ctr = dev->item_ctr + 2 * (dev->launches++ % ra::kItemCounterSlots);
   }
   // With fewer paired items than SMs the heaviest pair is the critical path:
   // one query tile per item halves it and fills the SMs better.

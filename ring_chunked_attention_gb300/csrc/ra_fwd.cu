@@ -46,6 +46,8 @@
 namespace ra {
 
 __device__ unsigned int g_status_word;
+// work-item counters: per slot the next unclaimed item and the CTAs done
+__device__ unsigned int g_item_ctr[2 * kItemCounterSlots];
 
 constexpr int kThreads = 384;
 constexpr uint32_t kLaunchRegs = 168, kSoftmaxRegs = 200, kProducerRegs = 104;
@@ -56,6 +58,13 @@ constexpr int kWarpMma = 9;
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr uint32_t kTmemCols = 512;
+// Work items are claimed at run time from a global counter (longest first) by
+// the producer thread.  The softmax warps take their ids from a ring of this
+// many entries in shared memory; the MMA thread reads each id from a word the
+// producer writes before arming the barrier of the item's first query tile,
+// which that thread waits for anyway.
+constexpr int kItemRing = 4;
+constexpr uint32_t kItemConsumers = 8;  // the eight softmax warps
 // Reference-max policy of the online softmax.  The reference max m is
 // refreshed only when a row's max grows by more than 2^8 (O is rescaled
 // rarely), and on tiles after a row's first the max pass is skipped unless a
@@ -90,9 +99,12 @@ struct Layout {
   // barrier indices
   static constexpr int Q_FULL = 0, Q_EMPTY = 2, K_FULL = 4, K_EMPTY = 4 + NS, V_FULL = 4 + 2 * NS,
                        V_EMPTY = 4 + 3 * NS, S_FULL = 4 + 4 * NS, P_FULL = 6 + 4 * NS,
-                       O_FREE = 8 + 4 * NS, DONE = 10 + 4 * NS, N_BARS = 11 + 4 * NS;
+                       O_FREE = 8 + 4 * NS, DONE = 10 + 4 * NS, ITEM_FULL = 11 + 4 * NS,
+                       ITEM_EMPTY = ITEM_FULL + kItemRing, N_BARS = ITEM_EMPTY + kItemRing;
   static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
-  static constexpr int BYTES = MISC_OFF + 16;
+  static constexpr int ITEM_OFF = MISC_OFF + 16;  // kItemRing work-item ids (softmax warps)
+  static constexpr int QID_OFF = ITEM_OFF + 4 * kItemRing;  // id of the item in query slot 0
+  static constexpr int BYTES = QID_OFF + 4;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
   __host__ __device__ static constexpr uint32_t S_COL(int i) { return 128u * i; }
   __host__ __device__ static constexpr uint32_t O_COL(int i) { return 256u + (uint32_t)OW * i; }
@@ -136,11 +148,16 @@ __device__ __forceinline__ Item decode_item(const FwdArgs& a, int x) {
   return it;
 }
 
-// k-th item of this CTA: snake order over rounds of gridDim.x items, so that
-// heaviest-first causal work balances across CTAs.
-__device__ __forceinline__ int item_index(int k) {
-  const int G = gridDim.x, c = blockIdx.x;
-  return k * G + ((k & 1) ? (G - 1 - c) : c);
+// plain 32-bit shared-memory accesses for the work-item ids (ordered by the
+// mbarrier arrive / wait that publishes them)
+__device__ __forceinline__ void st_shared_i32(uint32_t addr, int v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_shared_i32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ int qmax_of(const Item& it) {
@@ -224,6 +241,23 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// The k-th work item id of this CTA for a softmax warp (warp-collective call),
+// from the ring the producer fills; -1 when the sequence has ended or a wait
+// gave up.  The warp frees the ring entry at once.
+template <int D>
+__device__ __forceinline__ int next_item(const FwdArgs& a, uint32_t sbase, int k,
+                                         volatile int* abort_flag) {
+  using L = Layout<D>;
+  const int rs = k % kItemRing;
+  const uint32_t full = sbase + L::BAR_OFF + 8u * (L::ITEM_FULL + rs);
+  const uint32_t empty = sbase + L::BAR_OFF + 8u * (L::ITEM_EMPTY + rs);
+  if (!wait_warp(full, (uint32_t)(k / kItemRing) & 1u, abort_flag, a)) return -1;
+  const int x = ld_shared_i32(sbase + L::ITEM_OFF + 4 * rs);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(empty);
+  return x;
+}
+
 // ----------------------------------------------------------------- producer
 template <int D>
 __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
@@ -236,13 +270,43 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
   uint32_t kv_cnt = 0;  // steps whose K and V copies were both issued
   uint32_t k_cnt = 0;   // K copies issued (kv_cnt or kv_cnt + 1)
   bool ok = true;
+  // Work items are taken in order, longest first.  CTA c starts with item c;
+  // the items after the first gridDim.x are claimed from the launch's counter.
+  // The next claim is made when this thread reaches the current item's last
+  // key/value step: its latency hides behind the consumers' remaining steps,
+  // and an item goes to the CTA that is about to be free, so slower SMs claim
+  // fewer items.
+  const int first_claimed = (int)gridDim.x;
+  int claim = (int)blockIdx.x;
   for (int k = 0; ok; ++k) {
-    if (k * (int)gridDim.x >= a.n_items) break;
-    const int x = item_index(k);
-    if (x >= a.n_items) continue;
+    const int x = claim;
+    const int rs = k % kItemRing;
+    if (k >= kItemRing &&
+        !wait_bounded(bar(L::ITEM_EMPTY + rs), (uint32_t)((k / kItemRing) - 1) & 1u, abort_flag, a)) {
+      ok = false;
+      break;
+    }
+    st_shared_i32(sbase + L::ITEM_OFF + 4 * rs, x < a.n_items ? x : -1);
+    mbar_arrive(bar(L::ITEM_FULL + rs));  // release: the id is visible to whoever acquires it
+    if (x >= a.n_items) {
+      // the end, for the MMA thread: -1 in the slot-0 id word, through the
+      // slot's barrier (one arrival, no bytes) once the slot is free
+      if (q_cnt[0] > 0 &&
+          !wait_bounded(bar(L::Q_EMPTY + 0), (q_cnt[0] - 1) & 1, abort_flag, a)) {
+        ok = false;
+        break;
+      }
+      st_shared_i32(sbase + L::QID_OFF, -1);
+      mbar_arrive(bar(L::Q_FULL + 0));
+      ++q_cnt[0];
+      break;
+    }
     const Item it = decode_item(a, x);
     const int ns = n_steps(a, it);
-    if (ns == 0) continue;  // every key of the block is in the future of every row
+    if (ns == 0) {  // every key of the block is in the future of every row
+      claim = first_claimed + (int)atomicAdd(a.item_ctr, 1u);
+      continue;
+    }
 #pragma unroll
     for (int slot = 0; slot < 2 && ok; ++slot) {
       if (slot == 1 && !it.valid1) continue;
@@ -251,6 +315,7 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
         ok = false;
         break;
       }
+      if (slot == 0) st_shared_i32(sbase + L::QID_OFF, x);  // released by the arrive below
       mbar_arrive_expect_tx(bar(L::Q_FULL + slot), L::TILE);
       for (int kb = 0; kb < L::DK; ++kb)
         tma_load_3d(sbase + L::Q_OFF + slot * L::TILE + kb * L::BLOCK, tq, bar(L::Q_FULL + slot),
@@ -264,6 +329,7 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
       const int st = kv_cnt % L::NS;
       const uint32_t ph = (kv_cnt / L::NS) & 1;
       const int row = it.b * a.Sk + kt * kBN;
+      if (u == ns - 1) claim = first_claimed + (int)atomicAdd(a.item_ctr, 1u);  // the next item
       if (!wait_bounded(bar(L::K_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
       mbar_arrive_expect_tx(bar(L::K_FULL + st), L::TILE);
       for (int kb = 0; kb < L::DK; ++kb)
@@ -279,6 +345,9 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
       ++kv_cnt;
     }
   }
+  // the last claim has returned (its value is used here) before this CTA can
+  // count itself done and the last CTA resets the counter
+  asm volatile("" ::"r"(claim));
   if (!ok) {
     // Let every copy this thread issued land before shared memory goes away:
     // wait (bounded) for the last armed phase of each full barrier.
@@ -350,15 +419,14 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   uint32_t c = 0;                   // ring position of the current step
   bool ok = true;
 
-  for (int k = 0; ok; ++k) {
-    if (k * (int)gridDim.x >= a.n_items) break;
-    const int x = item_index(k);
-    if (x >= a.n_items) continue;
-    const Item it = decode_item(a, x);
-    const int ns = n_steps(a, it);
-    if (ns == 0) continue;
+  while (ok) {
+    // the next item with work: its id comes with its first query tile (-1: none left)
     if (!wait_bounded(bar(L::Q_FULL + 0), q_cnt0 & 1, abort_flag, a)) break;
     ++q_cnt0;
+    const int x = ld_shared_i32(sbase + L::QID_OFF);
+    if (x < 0) break;
+    const Item it = decode_item(a, x);
+    const int ns = n_steps(a, it);
     if (it.valid1) {
       if (!wait_bounded(bar(L::Q_FULL + 1), q_cnt1 & 1, abort_flag, a)) break;
       ++q_cnt1;
@@ -662,9 +730,8 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   uint32_t n = 0;  // S tiles consumed so far by this slot
 
   for (int k = 0;; ++k) {
-    if (k * (int)gridDim.x >= a.n_items) break;
-    const int x = item_index(k);
-    if (x >= a.n_items) continue;
+    const int x = next_item<D>(a, sbase, k, abort_flag);
+    if (x < 0) break;
     const Item it = decode_item(a, x);
     if (slot == 1 && !it.valid1) continue;
     // this slot's query tile and head, selected once: indexing the item with
@@ -765,7 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::N_BARS; ++i) {
       const bool per_warp = (i == L::P_FULL || i == L::P_FULL + 1);
-      mbar_init(sbase + L::BAR_OFF + 8u * i, per_warp ? 4u : 1u);
+      const bool item_free = (i >= L::ITEM_EMPTY && i < L::ITEM_EMPTY + kItemRing);
+      mbar_init(sbase + L::BAR_OFF + 8u * i, item_free ? kItemConsumers : (per_warp ? 4u : 1u));
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -810,6 +878,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // every claim of this CTA has returned (the producer used its last value
+  // before the barrier above); the last CTA to get here resets the counter
+  // for the next launch that uses this slot
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.item_ctr + 1, 1u) == gridDim.x - 1) {
+      volatile unsigned int* ctr = a.item_ctr;
+      ctr[0] = 0;
+      ctr[1] = 0;
+    }
+  }
 }
 
 size_t fwd_smem_bytes(int D) {
@@ -837,6 +916,10 @@ cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const FwdArgs& args, int grid, cudaStream_t stream) {
   if (D == 128) return launch_d<128>(tq, tk, tv, args, grid, stream);
   return launch_d<64>(tq, tk, tv, args, grid, stream);
+}
+
+cudaError_t item_counter_ptr(unsigned int** p) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_item_ctr);
 }
 
 cudaError_t status_word_ptr(unsigned int** p) {

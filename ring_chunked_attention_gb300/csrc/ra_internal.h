@@ -36,6 +36,7 @@ struct FwdArgs {
   unsigned long long timeout_ns;
   int skip_value_load;   // failure-path test hook
   int strict_mma_order;  // 1: wait for O_i += P_i V to complete before S_i is rewritten
+  unsigned int* item_ctr;  // this launch's work-item counter pair (next item, CTAs done), zero at launch
 };
 
 // Kernel arguments of the backward pass besides the tensor maps (q, k, v, dout).
@@ -70,6 +71,10 @@ cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const FwdArgs& args, int grid, cudaStream_t stream);
 size_t fwd_smem_bytes(int D);
 cudaError_t status_word_ptr(unsigned int** p);
+// Work-item counter slots of the forward (2 words each); a launch takes the
+// next slot in turn, so up to this many launches may run at once.
+constexpr int kItemCounterSlots = 64;
+cudaError_t item_counter_ptr(unsigned int** p);
 cudaError_t read_and_clear_status(unsigned int* value);
 
 // ra_bwd.cu

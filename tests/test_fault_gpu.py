@@ -30,6 +30,15 @@ def test_timeout_is_reported_and_context_survives(ralib, cuda_ok, oracle_mod):
     assert_parity(compare(out, lse, o_ref, l_ref), "after fault")
     x = torch.ones(1024, device="cuda")
     assert float((x * 2).sum()) == 2048.0
+    # the aborted launch left its work-item counter at zero too: the launch that
+    # takes the same counter again (64 launches later) claims every item
+    w2 = Workload("fault_claims", 1, 8, 2, 4096, 128, 4, True)  # more items than SMs
+    q2, k2, v2 = (t.cuda() for t in make_inputs(w2, seed=61))
+    o0, l0 = ralib.ra_fwd(q2, k2, v2, P=w2.P, causal=True)
+    for _ in range(65):
+        o, l = ralib.ra_fwd(q2, k2, v2, P=w2.P, causal=True)
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK
 
 
 @pytest.mark.parametrize("entry", ["ra_bwd", "ra_bwd_static"])

@@ -216,6 +216,46 @@ def test_late_dominant_key_takes_the_exact_path(ralib, cuda_ok, oracle_mod, D):
     assert (late - vt).abs().max().item() < 0.05
 
 
+def _claiming_workload():
+    """256 single-tile items on at most 152 SMs: every CTA claims items from the
+    launch's counter after its first."""
+    return Workload("claims", 1, 8, 2, 4096, 128, 4, True)
+
+
+def test_work_item_counters_cycle(ralib, cuda_ok):
+    """Each launch takes the next of the device's 64 work-item counters and the
+    kernel leaves it at zero; over more than two full cycles every launch
+    must claim every item exactly once, i.e. reproduce the first output."""
+    w = _claiming_workload()
+    q, k, v = (t.cuda() for t in make_inputs(w, seed=47))
+    o0, l0 = ralib.ra_fwd(q, k, v, P=w.P, causal=True)
+    out, lse = torch.empty_like(o0), torch.empty_like(l0)
+    for _ in range(130):
+        ralib.ra_fwd(q, k, v, P=w.P, causal=True, out=out, lse=lse)
+        torch.cuda.synchronize()
+        assert torch.equal(out, o0) and torch.equal(lse, l0)
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK
+
+
+def test_concurrent_launches_on_two_streams(ralib, cuda_ok):
+    """Two launches in flight at once on different streams use different
+    counters; each reproduces its own sequential result."""
+    w = _claiming_workload()
+    ins = [tuple(t.cuda() for t in make_inputs(w, seed=s)) for s in (53, 59)]
+    refs = [ralib.ra_fwd(*x, P=w.P, causal=True) for x in ins]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [(torch.empty_like(r[0]), torch.empty_like(r[1])) for r in refs]
+    for _ in range(5):
+        for x, s, (o, l) in zip(ins, streams, outs):
+            with torch.cuda.stream(s):
+                ralib.ra_fwd(*x, P=w.P, causal=True, out=o, lse=l, stream=s)
+        torch.cuda.synchronize()
+        for (o, l), (ro, rl) in zip(outs, refs):
+            assert torch.equal(o, ro) and torch.equal(l, rl)
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK
+
+
 def test_stream_argument_is_used(ralib, cuda_ok, oracle_mod):
     w = Workload("stream", 1, 4, 2, 512, 128, 2, True)
     q, k, v = make_inputs(w, seed=29)
