@@ -77,6 +77,10 @@ typedef enum ra_status {
  *   (scale == 0 is legal and gives uniform weights over the allowed keys)
  *   q, k, v, out 16-byte aligned; lse 4-byte aligned.
  *   out must not overlap q, k or v.
+ *   Range: finite inputs.  The fp32 accumulators hold weights of up to 2^30
+ *   per key tile relative to a running reference, so
+ *   2^30 * (S / 128) * max|v| must stay below 2^128 (|v| < 2^80 up to 16 M
+ *   keys); larger values can overflow to inf.
  * Returns RA_OK once the kernel is enqueued.  A kernel that had to give up a
  * bounded internal wait leaves out/lse partly written and records
  * RA_ERR_TIMEOUT for ra_get_last_device_status.

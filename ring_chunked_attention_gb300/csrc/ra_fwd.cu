@@ -85,7 +85,7 @@ struct SoftmaxPolicy {
 template <int D>
 struct Layout {
   static constexpr int DK = D / 64;                // 128-byte swizzle blocks per row
-  static constexpr int NS = (D == 128) ? 2 : 4;    // K/V ring depth
+  static constexpr int NS = (D == 128) ? 2 : 5;    // K/V ring depth
   static constexpr int BLOCK = 128 * 128;          // one [128 rows x 64 cols] bf16 block
   static constexpr int TILE = kBM * D * 2;         // one 128-row tile, all D
   static constexpr int Q_OFF = 0;
@@ -648,8 +648,9 @@ __device__ __forceinline__ float row_max(const uint32_t (&va)[32], const uint32_
 // The row's first tile sets the reference m to its max.  A later tile skips
 // the max pass: the exps run against the current m, and the tile's exact sum
 // tells whether any weight grew large (a tile sum <= 2^30 bounds every weight
-// by 2^30: representable in bf16, and O and l stay far from fp32 overflow;
-// the result is exact for any m since l and O share it).  Only when some row
+// by 2^30: representable in bf16, and over T key tiles l stays below 2^30 T
+// and O below 2^30 T max|v|, within fp32 while that is below 2^128; the
+// result is exact for any m since l and O share it).  Only when some row
 // of the warp exceeds that does the warp take the exact path, on the scores
 // read again from tensor memory (P is stored only once the weights are
 // accepted): row max, new reference where the max passed m + threshold, O

@@ -19,6 +19,8 @@ CASES = [
     ("noncausal_block", 1, 4, 4, 256, 640, 64, 0, 4096, False),
     ("single_tile_rows", 1, 3, 1, 128, 256, 128, 128, 0, True),
     ("diag_block_d64_qtiles", 1, 3, 3, 256, 384, 64, 256, 128, True),
+    # more work items than SMs (run-time claims), half of them with no allowed key
+    ("many_items_half_empty", 1, 8, 8, 4096, 2048, 128, 0, 2048, True),
 ]
 
 

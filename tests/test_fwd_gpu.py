@@ -190,17 +190,17 @@ def test_peaked_softmax_rescaling(ralib, cuda_ok, oracle_mod, D, sigma):
 
 @pytest.mark.parametrize("D", [64, 128])
 def test_late_dominant_key_takes_the_exact_path(ralib, cuda_ok, oracle_mod, D):
-    """One key of chunk 0 scores about 40 (natural units, 58 in log2 units)
+    """One key of chunk 0 scores about 50 (natural units, 72 in log2 units)
     above everything else for every row of chunks 1-3.  Those rows visit
     chunk 0 last in ring order, so by then their reference max is far below
     it: the speculative exps exceed the 2^30 guard and every such warp must
     take the exact path (scores streamed back from tensor memory, new
-    reference, O rescaled by about 2^-58).  The output is then dominated by
+    reference, O rescaled by about 2^-72).  The output is then dominated by
     that key's value row."""
     w = Workload("late", 1, 2, 1, 1024, D, 4, True)
     q, k, v = make_inputs(w, seed=31)
     t = 5                                   # the planted key (chunk 0, first tile)
-    amp = math.sqrt(40.0 * math.sqrt(D))    # amp^2 * scale = 40
+    amp = math.sqrt(50.0 * math.sqrt(D))    # amp^2 * scale = 50
     q = q.float()
     k = k.float()
     q[:, w.chunk:, :, 0] += amp             # rows of chunks 1..3 share a large first component
