@@ -12,7 +12,9 @@
 // CTA organisation (one CTA per SM, persistent over work items):
 //   warps 0-3  softmax + correction + epilogue for query slot 0 (TMEM lanes 0-127)
 //   warps 4-7  the same for query slot 1
-//   warp  8    TMA producer: Q tiles, then K/V tiles into an NS-stage ring
+//   warp  8    producer (one thread): claims the CTA's next work item at run
+//              time and hands its id on, then TMA-loads the Q tiles and the
+//              K/V tiles into an NS-stage ring
 //   warp  9    MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V
 //   warps 10-11 idle (they complete the producer warpgroup)
 // Registers are split with setmaxnreg: the launch gives every thread 168
@@ -21,7 +23,8 @@
 // warpgroup drops to 104 (2*128*200 + 128*104 = 384*168).
 // A work item is two 128-row query tiles sharing one key/value stream (two
 // heads of one GQA group, or two consecutive tiles of one head), so every
-// K/V tile staged in shared memory feeds two MMAs.
+// K/V tile staged in shared memory feeds two MMAs.  Items are handed out
+// longest first; a CTA claims its next one when it is about to be free.
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [  0,128) S_0   (P_0 as packed bf16 overwrites its first 64 columns)
