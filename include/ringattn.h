@@ -45,7 +45,9 @@ typedef enum ra_status {
                              non-finite scale, n < 1 */
   RA_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle: D not 64/128,
                              S/P not a multiple of 128, pointer not 16-byte aligned,
-                             negative scale, device is not sm_103, sizes past 2^31 rows */
+                             negative scale, device is not sm_103, sizes past 2^31 rows
+                             (ra_fwd, ra_fwd_block: past 2^30 128-row query tiles in
+                             B*H*S/128) */
   RA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute query,
                              tensor-map encode); ra_last_cuda_error() gives the code */
   RA_ERR_TIMEOUT = 4      /* a bounded wait inside a kernel gave up (reported by
@@ -217,7 +219,8 @@ const char* ra_status_string(ra_status s);
 /* The cudaError_t value behind the most recent RA_ERR_CUDA on this thread. */
 int ra_last_cuda_error(void);
 
-/* Library version, (major << 16) | (minor << 8) | patch. */
+/* Library version, (major << 16) | (minor << 8) | patch: 0.3.0 (0.3: the forward hands
+   out its work items at run time through per-device counters). */
 int ra_version(void);
 
 /*

@@ -243,7 +243,8 @@ ra_status ra_fwd(const void* q, const void* k, const void* v, void* out, float* 
   if ((S / P) % 128 != 0) return RA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_UNSUPPORTED;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return RA_ERR_UNSUPPORTED;
-  if ((long long)B * S >= (1ll << 31) || (long long)B * H * (S / 128) >= (1ll << 31))
+  // work-item ids, and the run-time claims past them, stay far inside int
+  if ((long long)B * S >= (1ll << 31) || (long long)B * H * (S / 128) >= (1ll << 30))
     return RA_ERR_UNSUPPORTED;
   return launch_attention(q, k, v, out, lse, B, H, Hkv, S, S, D, P, causal, scale, 0, 0, 0,
                           stream);
@@ -263,7 +264,7 @@ ra_status ra_fwd_block(const void* q, const void* k, const void* v, void* out, f
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_UNSUPPORTED;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return RA_ERR_UNSUPPORTED;
   if ((long long)B * Sq >= (1ll << 31) || (long long)B * Sk >= (1ll << 31) ||
-      (long long)B * H * (Sq / 128) >= (1ll << 31) || q_pos0 / 128 + Sq / 128 >= (1ll << 30) ||
+      (long long)B * H * (Sq / 128) >= (1ll << 30) || q_pos0 / 128 + Sq / 128 >= (1ll << 30) ||
       k_pos0 / 128 + Sk / 128 >= (1ll << 30))
     return RA_ERR_UNSUPPORTED;
   return launch_attention(q, k, v, out, lse, B, H, Hkv, Sq, Sk, D, 1, causal, scale, 1,
@@ -433,7 +434,7 @@ const char* ra_status_string(ra_status s) {
 
 int ra_last_cuda_error(void) { return g_last_cuda_error; }
 
-int ra_version(void) { return (0 << 16) | (2 << 8) | 0; }
+int ra_version(void) { return (0 << 16) | (3 << 8) | 0; }
 
 void ra_debug_set_fault(long long timeout_ns, int skip_value_load) {
   std::lock_guard<std::mutex> lock(g_mu);

@@ -34,7 +34,7 @@ def test_status_strings(ralib):
     assert ralib.ra_status_string(0) == "RA_OK"
     assert ralib.ra_status_string(4) == "RA_ERR_TIMEOUT"
     assert ralib.ra_status_string(99) == "RA_ERR_UNKNOWN"
-    assert ralib.ra_version() == (0 << 16) | (2 << 8)
+    assert ralib.ra_version() == (0 << 16) | (3 << 8)
 
 
 # Fake, 16-byte aligned addresses: validation must reject these calls before
@@ -62,6 +62,7 @@ def _call(ralib, q=Q, k=K, v=V, o=O, l=L, **kw):
     (dict(S=200, P=1), 2),             # ragged sequence
     (dict(q=Q + 8), 2), (dict(o=O + 4), 2), (dict(l=L + 2), 2),
     (dict(B=1 << 16, S=1 << 15, P=1), 2),  # B*S >= 2^31 rows
+    (dict(H=1 << 13, S=1 << 24, P=1), 2),  # 2^30 query tiles: work-item ids must stay in int
 ])
 def test_fwd_validation_rejects_before_launch(ralib, kw, code):
     assert _call(ralib, **kw) == code
@@ -85,6 +86,7 @@ def test_merge_validation_rejects_before_launch(ralib, kw, code):
     (dict(H=3, Hkv=2), 1), (dict(scale=float("nan")), 1),
     (dict(Sq=200), 2), (dict(Sk=100), 2), (dict(qp=64), 2), (dict(kp=1), 2), (dict(D=32), 2),
     (dict(scale=-1.0), 2), (dict(o=O + 4), 2),
+    (dict(H=1 << 13, Sq=1 << 24), 2),  # 2^30 query tiles
 ])
 def test_block_validation_rejects_before_launch(ralib, kw, code):
     a = dict(q=Q, k=K, v=V, o=O, l=L, B=1, H=4, Hkv=2, Sq=256, Sk=384, D=128, qp=256, kp=0,
