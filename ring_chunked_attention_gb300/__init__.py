@@ -103,6 +103,45 @@ def _check(code: int, what: str):
         raise RaError(code, what)
 
 
+def _dims(t, name: str, ndim: int):
+    """Shape of a tensor argument that must have ``ndim`` dimensions."""
+    import torch
+
+    if not isinstance(t, torch.Tensor) or t.dim() != ndim:
+        raise ValueError(f"{name} must be a {ndim}-D tensor")
+    return tuple(t.shape)
+
+
+def _tensor_checks(device, *specs):
+    """Each spec is (tensor, name, dtypes, shape or None).  The library reads
+    and writes these tensors by address on one device, so each must be a
+    contiguous CUDA tensor on ``device`` with one of the dtypes and the shape."""
+    import torch
+
+    for t, name, dtypes, shape in specs:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != device:
+            raise ValueError(f"{name} must be a CUDA tensor on {device}")
+        if t.dtype not in dtypes:
+            raise ValueError(f"{name} must have dtype {' or '.join(str(d) for d in dtypes)}, "
+                             f"got {t.dtype}")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+def _call_on(device, stream, fn):
+    """Run ``fn(stream_handle)`` with ``device`` current: the library launches
+    on the current device.  ``stream`` (default: that device's current
+    stream) must belong to the same device."""
+    import torch
+
+    with torch.cuda.device(device):
+        if stream is not None and hasattr(stream, "device") and stream.device != device:
+            raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+        return fn(_stream_ptr(stream))
+
+
 def ra_status_string(code: int) -> str:
     return _load().ra_status_string(int(code)).decode()
 
@@ -114,34 +153,31 @@ def ra_version() -> int:
 def ra_fwd(q, k, v, *, P: int, causal: bool, scale: float | None = None, out=None, lse=None,
            want_lse: bool = True, stream=None):
     """Ring-chunked attention forward.  ``q`` [B,S,H,D], ``k``/``v``
-    [B,S,Hkv,D] bf16 CUDA tensors (contiguous).  Returns ``(out, lse)`` with
-    ``out`` [B,S,H,D] bf16 and ``lse`` [B,H,S] fp32 (``None`` when
-    ``want_lse`` is false and no ``lse`` buffer is given).  ``scale``
-    defaults to 1/sqrt(D)."""
+    [B,S,Hkv,D] bf16 CUDA tensors (contiguous, one device).  Returns
+    ``(out, lse)`` with ``out`` [B,S,H,D] bf16 and ``lse`` [B,H,S] fp32
+    (``None`` when ``want_lse`` is false and no ``lse`` buffer is given).
+    ``scale`` defaults to 1/sqrt(D)."""
     import torch
 
     lib = _load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
-            raise ValueError(f"{n} must be a contiguous 4-D bf16 CUDA tensor")
-    B, S, H, D = q.shape
-    Hkv = k.shape[2]
-    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != (B, S, Hkv, D):
-        raise ValueError("k and v must be [B,S,Hkv,D] matching q")
+    B, S, H, D = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[2]
+    dev, bf = q.device, (torch.bfloat16,)
+    _tensor_checks(dev, (q, "q", bf, None), (k, "k", bf, (B, S, Hkv, D)),
+                   (v, "v", bf, (B, S, Hkv, D)))
     if scale is None:
         scale = D ** -0.5
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
-        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S)
-                            or not lse.is_contiguous()):
-        raise ValueError("lse must be a contiguous [B,H,S] fp32 tensor")
-    if tuple(out.shape) != (B, S, H, D) or out.dtype != torch.bfloat16 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous [B,S,H,D] bf16 tensor")
-    code = lib.ra_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                      None if lse is None else lse.data_ptr(), B, H, Hkv, S, D, int(P),
-                      int(bool(causal)), float(scale), _stream_ptr(stream))
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    _tensor_checks(dev, (out, "out", bf, (B, S, H, D)))
+    if lse is not None:
+        _tensor_checks(dev, (lse, "lse", (torch.float32,), (B, H, S)))
+    code = _call_on(dev, stream, lambda sp: lib.ra_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+        None if lse is None else lse.data_ptr(), B, H, Hkv, S, D, int(P), int(bool(causal)),
+        float(scale), sp))
     _check(code, "ra_fwd")
     return out, lse
 
@@ -155,23 +191,24 @@ def ra_fwd_block(q, k, v, *, q_pos0: int, k_pos0: int, causal: bool, scale: floa
     import torch
 
     lib = _load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
-            raise ValueError(f"{n} must be a contiguous 4-D bf16 CUDA tensor")
-    B, Sq, H, D = q.shape
-    Bk, Sk, Hkv, Dk = k.shape
-    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
-        raise ValueError("k and v must be [B,Sk,Hkv,D] matching q's B and D")
+    B, Sq, H, D = _dims(q, "q", 4)
+    _, Sk, Hkv, _ = _dims(k, "k", 4)
+    dev, bf = q.device, (torch.bfloat16,)
+    _tensor_checks(dev, (q, "q", bf, None), (k, "k", bf, (B, Sk, Hkv, D)),
+                   (v, "v", bf, (B, Sk, Hkv, D)))
     if scale is None:
         scale = D ** -0.5
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
-        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
-    code = lib.ra_fwd_block(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                            None if lse is None else lse.data_ptr(), B, H, Hkv, Sq, Sk, D,
-                            int(q_pos0), int(k_pos0), int(bool(causal)), float(scale),
-                            _stream_ptr(stream))
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+    _tensor_checks(dev, (out, "out", bf, (B, Sq, H, D)))
+    if lse is not None:
+        _tensor_checks(dev, (lse, "lse", (torch.float32,), (B, H, Sq)))
+    code = _call_on(dev, stream, lambda sp: lib.ra_fwd_block(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+        None if lse is None else lse.data_ptr(), B, H, Hkv, Sq, Sk, D, int(q_pos0), int(k_pos0),
+        int(bool(causal)), float(scale), sp))
     _check(code, "ra_fwd_block")
     return out, lse
 
@@ -190,32 +227,28 @@ def ra_bwd(q, k, v, out, lse, dout, *, P: int, causal: bool, scale: float | None
     import torch
 
     lib = _load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
-            raise ValueError(f"{n} must be a contiguous 4-D bf16 CUDA tensor")
-    B, S, H, D = q.shape
-    Hkv = k.shape[2]
-    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != (B, S, Hkv, D):
-        raise ValueError("k and v must be [B,S,Hkv,D] matching q")
-    if tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
-        raise ValueError("out and dout must have q's shape")
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous [B,H,S] fp32 tensor")
+    B, S, H, D = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[2]
+    dev, bf = q.device, (torch.bfloat16,)
+    _tensor_checks(dev, (q, "q", bf, None), (k, "k", bf, (B, S, Hkv, D)),
+                   (v, "v", bf, (B, S, Hkv, D)), (out, "out", bf, (B, S, H, D)),
+                   (dout, "dout", bf, (B, S, H, D)), (lse, "lse", (torch.float32,), (B, H, S)))
     if scale is None:
         scale = D ** -0.5
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for t, ref, n in ((dq, q, "dq"), (dk, k, "dk"), (dv, v, "dv")):
-        if t.dtype != torch.bfloat16 or tuple(t.shape) != tuple(ref.shape) or not t.is_contiguous():
-            raise ValueError(f"{n} must be a contiguous bf16 tensor shaped like its input")
+    _tensor_checks(dev, (dq, "dq", bf, (B, S, H, D)), (dk, "dk", bf, (B, S, Hkv, D)),
+                   (dv, "dv", bf, (B, S, Hkv, D)))
     need = ra_bwd_workspace_bytes(B, H, S)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    code = lib.ra_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                      dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                      workspace.data_ptr(), workspace.numel() * workspace.element_size(), B, H, Hkv,
-                      S, D, int(P), int(bool(causal)), float(scale), _stream_ptr(stream))
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _tensor_checks(dev, (workspace, "workspace", (workspace.dtype,), None))
+    code = _call_on(dev, stream, lambda sp: lib.ra_bwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+        dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), B, H, Hkv, S, D, int(P),
+        int(bool(causal)), float(scale), sp))
     _check(code, "ra_bwd")
     return dq, dk, dv
 
@@ -228,25 +261,20 @@ def ra_bwd_static(q, k, v, out, lse, dout, dq, dk, dv, *, P: int, causal: bool,
     import torch
 
     lib = _load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"),
-                 (dk, "dk"), (dv, "dv")):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
-            raise ValueError(f"{n} must be a contiguous 4-D bf16 CUDA tensor")
-    B, S, H, D = q.shape
-    Hkv = k.shape[2]
-    if (tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != tuple(k.shape)
-            or tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape)
-            or tuple(dq.shape) != tuple(q.shape) or tuple(dk.shape) != tuple(k.shape)
-            or tuple(dv.shape) != tuple(k.shape)):
-        raise ValueError("shapes must match ra_bwd's")
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous [B,H,S] fp32 tensor")
+    B, S, H, D = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[2]
+    dev, bf = q.device, (torch.bfloat16,)
+    _tensor_checks(dev, (q, "q", bf, None), (k, "k", bf, (B, S, Hkv, D)),
+                   (v, "v", bf, (B, S, Hkv, D)), (out, "out", bf, (B, S, H, D)),
+                   (dout, "dout", bf, (B, S, H, D)), (lse, "lse", (torch.float32,), (B, H, S)),
+                   (dq, "dq", bf, (B, S, H, D)), (dk, "dk", bf, (B, S, Hkv, D)),
+                   (dv, "dv", bf, (B, S, Hkv, D)))
     if scale is None:
         scale = D ** -0.5
-    code = lib.ra_bwd_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                             lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                             dv.data_ptr(), B, H, Hkv, S, D, int(P), int(bool(causal)),
-                             float(scale), _stream_ptr(stream))
+    code = _call_on(dev, stream, lambda sp: lib.ra_bwd_static(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+        dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, S, D, int(P),
+        int(bool(causal)), float(scale), sp))
     _check(code, "ra_bwd_static")
     return dq, dk, dv
 
@@ -266,22 +294,20 @@ def ra_merge_partials(o_parts, lse_parts, *, out=None, lse=None, want_lse: bool 
     import torch
 
     lib = _load()
-    if o_parts.dim() != 5 or not o_parts.is_cuda or not o_parts.is_contiguous():
-        raise ValueError("o_parts must be a contiguous [n,B,S,H,D] CUDA tensor")
-    if o_parts.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("o_parts must be bf16 or fp32")
-    n, B, S, H, D = o_parts.shape
-    if (lse_parts.dtype != torch.float32 or tuple(lse_parts.shape) != (n, B, H, S)
-            or not lse_parts.is_contiguous()):
-        raise ValueError("lse_parts must be a contiguous [n,B,H,S] fp32 tensor")
+    n, B, S, H, D = _dims(o_parts, "o_parts", 5)
+    dev = o_parts.device
+    _tensor_checks(dev, (o_parts, "o_parts", (torch.bfloat16, torch.float32), None),
+                   (lse_parts, "lse_parts", (torch.float32,), (n, B, H, S)))
     if out is None:
-        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=o_parts.device)
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
     if lse is None and want_lse:
-        lse = torch.empty((B, H, S), dtype=torch.float32, device=o_parts.device)
-    code = lib.ra_merge_partials(o_parts.data_ptr(), int(o_parts.dtype == torch.float32),
-                                 lse_parts.data_ptr(), n, out.data_ptr(),
-                                 None if lse is None else lse.data_ptr(), B, H, S, D,
-                                 _stream_ptr(stream))
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    _tensor_checks(dev, (out, "out", (torch.bfloat16,), (B, S, H, D)))
+    if lse is not None:
+        _tensor_checks(dev, (lse, "lse", (torch.float32,), (B, H, S)))
+    code = _call_on(dev, stream, lambda sp: lib.ra_merge_partials(
+        o_parts.data_ptr(), int(o_parts.dtype == torch.float32), lse_parts.data_ptr(), n,
+        out.data_ptr(), None if lse is None else lse.data_ptr(), B, H, S, D, sp))
     _check(code, "ra_merge_partials")
     return out, lse
 

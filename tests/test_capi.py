@@ -123,3 +123,27 @@ def test_bwd_validation_rejects_before_launch(ralib, kw, code):
                     a["ws"], a["ws_bytes"], a["B"], a["H"], a["Hkv"], a["S"], a["D"], a["P"],
                     a["causal"], a["scale"], None)
     assert rc == code
+
+
+def test_binding_rejects_tensors_it_cannot_hand_to_the_device(ralib):
+    """The binding passes raw addresses, so a tensor that is not a CUDA tensor
+    on the inputs' device, or has the wrong rank, must be refused before any
+    CUDA call (on a host without a GPU every tensor here is a CPU tensor)."""
+    import torch
+
+    q = torch.zeros(1, 256, 2, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 256)
+    with pytest.raises(ValueError):
+        ralib.ra_fwd(q, q, q, P=1, causal=True)
+    with pytest.raises(ValueError):
+        ralib.ra_fwd(q[0], q, q, P=1, causal=True)  # 3-D q
+    with pytest.raises(ValueError):
+        ralib.ra_fwd_block(q, q, q, q_pos0=0, k_pos0=0, causal=True)
+    with pytest.raises(ValueError):
+        ralib.ra_bwd(q, q, q, q, lse, q, P=1, causal=True)
+    with pytest.raises(ValueError):
+        ralib.ra_bwd_static(q, q, q, q, lse, q, q, q, q, P=1, causal=True)
+    with pytest.raises(ValueError):
+        ralib.ra_merge_partials(q[None], lse[None])
+    with pytest.raises(ValueError):
+        ralib.ra_merge_partials(q, lse)  # 4-D partials

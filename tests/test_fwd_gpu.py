@@ -256,6 +256,33 @@ def test_concurrent_launches_on_two_streams(ralib, cuda_ok):
     assert ralib.ra_get_last_device_status() == ralib.RA_OK
 
 
+def test_binding_checks_caller_buffers(ralib, cuda_ok):
+    """Caller-provided outputs must be CUDA tensors of the right shape and dtype
+    on the inputs' device: the kernels write them by address."""
+    w = Workload("bufs", 1, 2, 2, 256, 64, 2, True)
+    q, k, v = (t.cuda() for t in make_inputs(w, seed=67))
+    with pytest.raises(ValueError):
+        ralib.ra_fwd(q, k, v, P=w.P, causal=True, out=torch.empty(q.shape, dtype=q.dtype))
+    with pytest.raises(ValueError):
+        ralib.ra_fwd(q, k, v, P=w.P, causal=True, lse=torch.empty(1, 2, 256))
+    with pytest.raises(ValueError):
+        ralib.ra_fwd(q, k, v, P=w.P, causal=True, out=torch.empty_like(q)[:, :128])
+    with pytest.raises(ValueError):
+        ralib.ra_fwd_block(q, k, v, q_pos0=0, k_pos0=0, causal=True,
+                           out=torch.empty(1, 128, 2, 64, dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        ralib.ra_fwd_block(q, k, v, q_pos0=0, k_pos0=0, causal=True,
+                           lse=torch.empty(1, 2, 256, dtype=torch.float64, device="cuda"))
+    out, lse = ralib.ra_fwd(q, k, v, P=w.P, causal=True)
+    with pytest.raises(ValueError):
+        ralib.ra_bwd(q, k, v, out, lse, torch.randn_like(q), P=w.P, causal=True,
+                     workspace=torch.empty(1 << 16, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        ralib.ra_merge_partials(out[None].float(), lse[None], out=torch.empty_like(out).float())
+    torch.cuda.synchronize()
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK
+
+
 def test_stream_argument_is_used(ralib, cuda_ok, oracle_mod):
     w = Workload("stream", 1, 4, 2, 512, 128, 2, True)
     q, k, v = make_inputs(w, seed=29)
