@@ -22,6 +22,14 @@ ra_status cuda_fail(cudaError_t e) {
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
 std::mutex g_mu;
+
+}  // namespace
+
+namespace ra {
+std::atomic<unsigned> g_prep_epoch{0};
+}  // namespace ra
+
+namespace {
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 int g_skip_value_load = 0;
 int g_strict_mma_order = 0;
@@ -454,6 +462,7 @@ void ra_set_item_pairing(int policy) {
 
 void ra_shutdown(void) {
   std::lock_guard<std::mutex> lock(g_mu);
+  ra::g_prep_epoch.fetch_add(1u, std::memory_order_acq_rel);  // kernels are prepared again
   for (auto& e : g_maps) e.used = false;
   for (auto& d : g_dev) d = DeviceInfo{};
   g_timeout_ns = kDefaultTimeoutNs;

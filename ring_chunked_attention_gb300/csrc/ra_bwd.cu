@@ -881,17 +881,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// `prepared`: this kernel's per-device preparation state (see prepare_kernel)
 template <class Kernel>
-cudaError_t launch_tc(Kernel kernel, int smem, int grid, cudaStream_t stream, const CUtensorMap& tq,
-                      const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                      const BwdArgs& args) {
-  // the setmaxnreg split is sized for exactly kBwdLaunchRegs registers per
-  // thread at launch; any other allocation would make setmaxnreg.inc wait forever
-  cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
-  if (e != cudaSuccess) return e;
-  if (attr.numRegs != (int)kBwdLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t launch_tc(Kernel kernel, int smem, std::atomic<unsigned>* prepared, int grid,
+                      cudaStream_t stream, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args) {
+  const cudaError_t e = prepare_kernel(kernel, (int)kBwdLaunchRegs, smem, prepared);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, args);
   return cudaGetLastError();
@@ -921,17 +916,23 @@ cudaError_t launch_bwd_prep(int D, const BwdArgs& args, int grid, cudaStream_t s
 cudaError_t launch_bwd_dkdv(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
                             int grid, cudaStream_t stream) {
+  static std::atomic<unsigned> prepared128[kMaxPrepDevices], prepared64[kMaxPrepDevices];
   if (D == 128)
-    return launch_tc(bwd_dkdv_kernel<128>, KvLayout<128>::ALLOC, grid, stream, tq, tk, tv, tdo, args);
-  return launch_tc(bwd_dkdv_kernel<64>, KvLayout<64>::ALLOC, grid, stream, tq, tk, tv, tdo, args);
+    return launch_tc(bwd_dkdv_kernel<128>, KvLayout<128>::ALLOC, prepared128, grid, stream, tq, tk,
+                     tv, tdo, args);
+  return launch_tc(bwd_dkdv_kernel<64>, KvLayout<64>::ALLOC, prepared64, grid, stream, tq, tk, tv,
+                   tdo, args);
 }
 
 cudaError_t launch_bwd_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
                           int grid, cudaStream_t stream) {
+  static std::atomic<unsigned> prepared128[kMaxPrepDevices], prepared64[kMaxPrepDevices];
   if (D == 128)
-    return launch_tc(bwd_dq_kernel<128>, DqLayout<128>::ALLOC, grid, stream, tq, tk, tv, tdo, args);
-  return launch_tc(bwd_dq_kernel<64>, DqLayout<64>::ALLOC, grid, stream, tq, tk, tv, tdo, args);
+    return launch_tc(bwd_dq_kernel<128>, DqLayout<128>::ALLOC, prepared128, grid, stream, tq, tk,
+                     tv, tdo, args);
+  return launch_tc(bwd_dq_kernel<64>, DqLayout<64>::ALLOC, prepared64, grid, stream, tq, tk, tv,
+                   tdo, args);
 }
 
 }  // namespace ra

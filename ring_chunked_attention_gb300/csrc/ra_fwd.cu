@@ -903,14 +903,8 @@ template <int D>
 static cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdArgs& args, int grid, cudaStream_t stream) {
   const int smem = Layout<D>::ALLOC;
-  // the setmaxnreg split is sized for exactly kLaunchRegs registers per thread
-  // at launch; any other allocation would make setmaxnreg.inc wait forever
-  cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, ring_attn_fwd_kernel<D>);
-  if (e != cudaSuccess) return e;
-  if (attr.numRegs != (int)kLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(ring_attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem);
+  static std::atomic<unsigned> prepared[kMaxPrepDevices];
+  const cudaError_t e = prepare_kernel(ring_attn_fwd_kernel<D>, (int)kLaunchRegs, smem, prepared);
   if (e != cudaSuccess) return e;
   ring_attn_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
   return cudaGetLastError();

@@ -3,6 +3,8 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
 
 namespace ra {
@@ -71,6 +73,35 @@ cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const FwdArgs& args, int grid, cudaStream_t stream);
 size_t fwd_smem_bytes(int D);
 cudaError_t status_word_ptr(unsigned int** p);
+
+// Host side: a tensor-core kernel's register count is checked (its setmaxnreg
+// split is sized for exactly `regs` registers per thread at launch; any other
+// allocation would make setmaxnreg.inc wait forever) and its dynamic
+// shared-memory limit raised once per device and kernel.  Both persist on the
+// function, so later launches, including launches recorded into a CUDA graph,
+// make no attribute calls.  `prepared[dev]` holds the preparation epoch + 1;
+// ra_shutdown starts a new epoch (after a device reset, call ra_shutdown).
+constexpr int kMaxPrepDevices = 64;
+extern std::atomic<unsigned> g_prep_epoch;
+
+template <class Kernel>
+inline cudaError_t prepare_kernel(Kernel kernel, int regs, int smem,
+                                  std::atomic<unsigned>* prepared) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cache = dev >= 0 && dev < kMaxPrepDevices;
+  const unsigned mark = g_prep_epoch.load(std::memory_order_acquire) + 1u;
+  if (cache && prepared[dev].load(std::memory_order_acquire) == mark) return cudaSuccess;
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, kernel);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != regs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (cache) prepared[dev].store(mark, std::memory_order_release);
+  return cudaSuccess;
+}
 // Work-item counter slots of the forward (2 words each); a launch takes the
 // next slot in turn, so up to this many launches may run at once.
 constexpr int kItemCounterSlots = 64;

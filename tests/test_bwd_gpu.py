@@ -263,3 +263,33 @@ def test_workspace_is_caller_owned_and_reusable(ralib, cuda_ok):
         assert torch.equal(x, y)
     with pytest.raises(ralib.RaError):
         ralib.ra_bwd(qd, kd, vd, out, lse, dod, P=w.P, causal=True, workspace=ws[:-16])
+
+
+def test_cuda_graph_capture_and_replay(ralib, cuda_ok):
+    """ra_bwd (three kernels) recorded into a CUDA graph replays to the eager
+    gradients: its launches make no attribute calls once the kernels are
+    prepared."""
+    w = Workload("graph", 1, 8, 2, 1024, 128, 4, True)
+    q, k, v = (t.cuda() for t in make_inputs(w, seed=79))
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(80)).bfloat16().cuda()
+    out, lse = ralib.ra_fwd(q, k, v, P=w.P, causal=True)
+    ref = ralib.ra_bwd(q, k, v, out, lse, do, P=w.P, causal=True)
+    dq, dk, dv = (torch.empty_like(t) for t in ref)
+    ws = torch.empty(ralib.ra_bwd_workspace_bytes(w.B, w.H, w.S), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ralib.ra_bwd(q, k, v, out, lse, do, P=w.P, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ralib.ra_bwd(q, k, v, out, lse, do, P=w.P, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+    for _ in range(3):
+        for t in (dq, dk, dv):
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for got, r in zip((dq, dk, dv), ref):
+            assert torch.equal(got, r)
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK

@@ -256,6 +256,46 @@ def test_concurrent_launches_on_two_streams(ralib, cuda_ok):
     assert ralib.ra_get_last_device_status() == ralib.RA_OK
 
 
+def test_cuda_graph_capture_and_replay(ralib, cuda_ok):
+    """ra_fwd recorded into a CUDA graph replays to the eager result, again and
+    again: the launch makes no attribute calls once its kernel is prepared, and
+    the captured launch's work-item counter is back at zero after each replay
+    (this workload has more items than SMs, so every replay claims items)."""
+    w = _claiming_workload()
+    q, k, v = (t.cuda() for t in make_inputs(w, seed=71))
+    ref_o, ref_l = ralib.ra_fwd(q, k, v, P=w.P, causal=True)
+    out, lse = torch.empty_like(ref_o), torch.empty_like(ref_l)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up on the capture stream's device
+        ralib.ra_fwd(q, k, v, P=w.P, causal=True, out=out, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ralib.ra_fwd(q, k, v, P=w.P, causal=True, out=out, lse=lse)
+    for _ in range(4):
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK
+
+
+def test_launches_after_shutdown(ralib, cuda_ok):
+    """ra_shutdown drops the host caches and starts a new kernel-preparation
+    epoch; the next launches prepare again and give the same result."""
+    w = Workload("shut", 1, 4, 2, 512, 128, 2, True)
+    q, k, v = (t.cuda() for t in make_inputs(w, seed=73))
+    o1, l1 = ralib.ra_fwd(q, k, v, P=w.P, causal=True)
+    ralib.ra_shutdown()
+    o2, l2 = ralib.ra_fwd(q, k, v, P=w.P, causal=True)
+    torch.cuda.synchronize()
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_binding_checks_caller_buffers(ralib, cuda_ok):
     """Caller-provided outputs must be CUDA tensors of the right shape and dtype
     on the inputs' device: the kernels write them by address."""
