@@ -262,7 +262,11 @@ void ra_set_mma_order(int strict);
  */
 void ra_set_item_pairing(int policy);
 
-/* Drop cached tensor maps and device queries (no device memory is held). */
+/* Drop cached tensor maps and device queries and reset the debug and policy
+ * settings (no device memory is held).  Each kernel's launch attributes are
+ * set once per device and then reused, which also lets ra_fwd, ra_fwd_block
+ * and ra_bwd be recorded into CUDA graphs; after a device reset
+ * (cudaDeviceReset), call ra_shutdown so that they are set again. */
 void ra_shutdown(void);
 
 #ifdef __cplusplus
