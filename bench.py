@@ -357,6 +357,62 @@ def measure_bwd(ra, w, flush, stream, qd, kd, vd, out, lse, steps: int = 10):
             "peak_source": f"{src} bf16 dense burst"}
 
 
+def measure_others(ra, flush, stream, names, steps: int = 5, warmup: int = 2):
+    """Device-timed ra_fwd on the other long-context workloads (the forward
+    only): median of ``steps`` launches after ``warmup``, L2 flushed before
+    each, CUDA events on the launch stream.  Returns {name: {...}}."""
+    import torch
+
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    res = {}
+    for name in names:
+        w = WORKLOADS[name]
+        q, k, v = (t.cuda() for t in make_inputs(w))
+        out = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+        ts = []
+        for i in range(warmup + steps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ra.ra_fwd(q, k, v, P=w.P, causal=w.causal, scale=w.scale, out=out, lse=lse,
+                      stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= warmup:
+                ts.append(e0.elapsed_time(e1))
+        if ra.ra_get_last_device_status() != 0:
+            raise RuntimeError(f"device status reported a timeout on {name}")
+        ms = statistics.median(ts)
+        tf = w.flops / (ms * 1e-3) / 1e12
+        res[name] = {"ms": ms, "tflops": tf, "frac": tf / peak, "launches": steps,
+                     "config": {"B": w.B, "H": w.H, "Hkv": w.Hkv, "S": w.S, "D": w.D, "P": w.P,
+                                "causal": w.causal}}
+        del q, k, v, out, lse
+        torch.cuda.empty_cache()
+    return res
+
+
+def ceilings_obj(ra, tensor_peak: float):
+    """The secondary ceilings beside the tensor roofline, measured on this
+    device by the library's microbenchmarks: the rate of ex2 (one per allowed
+    pair) and of fp32 FMA-pipe lanes (the kernel's instruction mix spends
+    three per pair at D = 128: one fma for the exponent's argument and two
+    adds for the exact and the rounded row sums; two at D = 64, where the
+    tensor cores take the rounded sum).  Each is converted to the forward
+    TFLOP/s it would allow alone (4*D FLOP per pair)."""
+    c = ra.ra_measure_ceilings()
+    out = {"measured": c, "tensor_peak_tflops": tensor_peak}
+    for D, lanes in ((128, 3.0), (64, 2.0)):
+        out[f"d{D}"] = {
+            "ex2_bound_tflops": c["ex2_per_s"] * 4 * D / 1e12,
+            "fp32_lanes_per_pair": lanes,
+            "fp32_bound_tflops": c["ffma2_lanes_per_s"] / lanes * 4 * D / 1e12,
+        }
+    return out
+
+
 def measure_e2e(ra, w, q, k, v, flush, steps: int):
     """End to end through ra_fwd with the inputs in pinned host memory: every
     step copies its q, k, v host -> device, runs the forward and reads out and
@@ -435,6 +491,7 @@ def run_ours(args):
     rab.build()  # no-op once built; fails loudly if the toolchain is missing
 
     w = WORKLOADS[args.workload]
+    ra.ra_set_mma_order(args.mma_order)
     q, k, v = make_inputs(w)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     out = torch.empty_like(qd)
@@ -480,6 +537,12 @@ def run_ours(args):
     e2e_ms, h2d, d2h, e2e_steps = measure_e2e(ra, w, q, k, v, flush, max(10, min(args.steps, 30)))
 
     merge = None if args.no_merge else measure_merge(ra, w, flush, stream)
+    others = None
+    if not args.no_others:
+        others = measure_others(ra, flush, stream,
+                                [n for n in ("causal_s4096", "long_s65536", "d64_s32768")
+                                 if n != w.name])
+    ceilings = None if args.no_ceilings else ceilings_obj(ra, float(load_peaks()[0]["bf16_tflops"]))
     bwd = None if args.no_bwd else measure_bwd(ra, w, flush, stream, qd, kd, vd, out, lse)
 
     # slowest rank decides
@@ -526,6 +589,114 @@ def run_ours(args):
             "kernel_sha": kernel_sha(),
             "merge": merge,
             "bwd": bwd,
+            "others": others,
+            "ceilings": ceilings,
+            "mma_order": args.mma_order,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_ring(args):
+    """Ring attention across ranks: the workload's sequence is sharded over the
+    N ranks (one GPU each, torchrun, NCCL point-to-point for the key/value
+    blocks), or over ``--virtual-ranks`` ranks emulated on one GPU.  One step
+    = the whole ring forward of every rank; value = the attention FLOPs of the
+    whole sequence over the slowest rank's step time (strong scaling: the
+    total work is fixed as N grows)."""
+    import torch
+
+    import ring_chunked_attention_gb300 as ra
+    from ring_chunked_attention_gb300 import build as rab
+    from ring_chunked_attention_gb300.ring import (RingSpec, block_plan, ring_attention, shard,
+                                                   virtual_ring_attention)
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    if rank == 0:
+        rab.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    rab.build()
+    ra.ra_set_mma_order(args.mma_order)
+    w = WORKLOADS[args.workload]
+    virtual = ws == 1 and args.virtual_ranks > 1
+    world = args.virtual_ranks if virtual else ws
+    spec = RingSpec(world, w.B, w.H, w.Hkv, w.S, w.D, w.causal, args.ring)
+    q, k, v = make_inputs(w)
+    mine = range(world) if virtual else [rank]
+    qs = [shard(q, spec, r).cuda() for r in mine]
+    ks = [shard(k, spec, r).cuda() for r in mine]
+    vs = [shard(v, spec, r).cuda() for r in mine]
+    del q, k, v
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    launches = 0
+    for r in mine:
+        steps, counts = block_plan(spec, r)
+        launches += sum(len(p) for _, p in steps) + sum(1 for c in counts if c > 1)
+
+    def step():
+        if virtual:
+            virtual_ring_attention(qs, ks, vs, causal=w.causal, layout=args.ring)
+        else:
+            ring_attention(qs[0], ks[0], vs[0], causal=w.causal, layout=args.ring, S=w.S)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if ra.ra_get_last_device_status() != 0:
+        raise RuntimeError("device status after warm-up reported a timeout")
+    sampler = ClockSampler(torch.cuda.current_device())
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.5)
+    t_start = time.time()
+    ts = []
+    for _ in range(args.steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    sampler.mark(t_start, time.time())
+    clocks = sampler.stop()
+    if ra.ra_get_last_device_status() != 0:
+        raise RuntimeError("device status reported a timeout in the timed region")
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ts)
+    (ms,) = max_over_ranks([ms], device="cuda")
+    value = w.flops / (ms * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "mode": "ring", "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv,
+                                       "S": w.S, "D": w.D, "causal": w.causal,
+                                       "flops_per_step": w.flops, "ring_layout": args.ring,
+                                       "ranks": world, "virtual_ranks": virtual,
+                                       "l2": "flushed between timed steps (256 MiB write)",
+                                       "parallelism": f"sequence ring x{world}"},
+            "roofline": {"bound": "tensor", "achieved": value / max(1, ws), "peak": peak,
+                         "unit": UNIT, "frac": value / max(1, ws) / peak,
+                         "peak_source": f"{src} bf16 dense burst", "traffic": None},
+            "gpu_launches": launches * args.steps, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -545,6 +716,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-merge", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the forward timing of the other long-context workloads")
+    ap.add_argument("--no-ceilings", action="store_true",
+                    help="skip the ex2 / fp32 microbenchmarks")
+    ap.add_argument("--ring", choices=["contiguous", "zigzag"], default=None,
+                    help="shard the sequence over the ranks (ring attention across GPUs) "
+                         "instead of running one replica per rank")
+    ap.add_argument("--virtual-ranks", type=int, default=0,
+                    help="with --ring on one GPU: emulate this many ranks in one process")
+    ap.add_argument("--mma-order", type=int, default=0, choices=[0, 1, 2],
+                    help="forward MMA issue order (0 grouped, the default; 1 strict; 2 in-order)")
     ap.add_argument("--full-oracle", action="store_true",
                     help="time the CPU oracle on every row of the workload instead of a sample "
                          "(minutes at the long-context sizes)")
@@ -553,6 +735,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.ring:
+        return run_ring(args)
     return run_ours(args)
 
 

@@ -17,14 +17,20 @@
  *   - Every pointer to tensor data is a DEVICE pointer into memory the caller
  *     owns; the library never allocates, frees or retains caller memory.  The
  *     only library-owned device state is one status word per device (see
- *     ra_get_last_device_status), 64 work-item counters per device for the
- *     forward kernel, the static scratch of ra_bwd_static, and the kernels' code.
+ *     ra_get_last_device_status), 4096 work-item counters per device for the
+ *     forward kernel (32 KiB), the static scratch of ra_bwd_static, and the
+ *     kernels' code.
  *   - ra_fwd and ra_fwd_block hand out their work items at run time through a
- *     counter that each launch takes in turn from the device's 64 and leaves at
- *     zero when it ends: up to 64 of these launches may be in flight on one
- *     device at once (on any streams).  A launch captured into a CUDA graph
- *     keeps its counter, so one captured launch must not run concurrently
- *     with itself (replays of it in one stream are fine).
+ *     counter in device memory that the launch leaves at zero when it ends.
+ *     Eager launches take the device's 64 eager counters in turn: up to 64
+ *     eager launches may be in flight on one device at once (on any streams).
+ *     A launch recorded into a CUDA graph (its stream is capturing) keeps a
+ *     counter of its own for every replay, one that no other launch of this
+ *     process is ever given, so replays can run beside any eager launches and
+ *     beside other graphs; one captured launch must not run concurrently with
+ *     itself (replays of one graph in one stream are fine).  A process can
+ *     record at most 4032 launches per device; later captures get
+ *     RA_ERR_UNSUPPORTED.  ra_shutdown does not restart either sequence.
  *   - Every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and returns without waiting; results are valid once the
  *     stream has reached the work.
@@ -124,7 +130,9 @@ ra_status ra_fwd_block(const void* q, const void* k, const void* v, void* out, f
  *             partial k holds O_k = (sum over its keys of e^{x_t} v_t) /
  *             (sum over its keys of e^{x_t}), as ra_fwd writes it
  *   lse_parts [n, B, H, S]     fp32; lse_k = ln(sum over its keys of e^{x_t});
- *             -inf marks a partial with no key, which contributes nothing
+ *             -inf marks a partial with no key, which contributes nothing (its
+ *             o_parts entries are not read); every other lse_k must be finite
+ *             (+inf or NaN make that row's out and lse NaN)
  *   out       [B, S, H, D]     bf16, written: sum_k e^{lse_k - lse} O_k
  *   lse       [B, H, S]        fp32, written: ln sum_k e^{lse_k}; may be NULL
  *   When every lse_k of a row is -inf the row gets out = 0 and lse = -inf.
@@ -213,6 +221,25 @@ ra_status ra_bwd_static(const void* q, const void* k, const void* v, const void*
  */
 ra_status ra_get_last_device_status(void* stream);
 
+/*
+ * ra_measure_ceilings -- measure, on the current device, the two non-tensor
+ * rates the forward's online softmax depends on (no counterpart on the pages;
+ * a diagnostic of this library).  Per allowed (query, key) pair the softmax
+ * computes one exp2 on the MUFU unit and a few fp32 operations, so these
+ * rates bound the pairs per second beside the tensor-core roofline.
+ * Runs microbenchmark kernels (one 1024-thread CTA per SM, about a
+ * millisecond in all) on a stream of its own and waits for them; allocates
+ * nothing (its timing records live in a 20 KiB library-owned device array).
+ *   out[8] host doubles, written:
+ *     [0] ex2 results per SM per clock      [1] ex2 results per second (whole GPU)
+ *     [2] scalar fp32 FMA lanes / SM / clk  [3] scalar fp32 FMA lanes per second
+ *     [4] packed f32x2 FMA lanes / SM / clk [5] packed f32x2 FMA lanes per second
+ *     [6] mean SM clock during the runs (MHz) [7] SMs measured
+ * Returns RA_ERR_INVALID_ARG for a NULL out, RA_ERR_UNSUPPORTED off sm_103,
+ * RA_ERR_CUDA if a launch or copy fails.
+ */
+ra_status ra_measure_ceilings(double* out);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* ra_status_string(ra_status s);
 
@@ -235,19 +262,27 @@ int ra_version(void);
 void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
 
 /*
- * MMA issue order of ra_fwd (no counterpart on the pages; an implementation
- * choice of this library).  The probabilities P_i of a query tile are kept in
- * tensor memory over the columns of the score tile S_i that produced them.
- * By default (strict == 0) the next S_i = Q_i K^T is issued right behind
- * O_i += P_i V from the same thread, relying on the tensor pipe executing one
- * thread's MMAs in issue order (as an in-order pipe does); this keeps the
- * pipe full.  With strict != 0 the issuing thread waits for that PV to
- * complete before S_i is rewritten, the ordering the PTX ISA guarantees for
- * MMAs on different accumulators, at the cost of a pipe drain per tile.  Both
- * orders compute the same arithmetic; the test-suite checks that their
- * outputs are bit-identical.  Applies to launches made after the call.
+ * MMA issue order of ra_fwd and ra_fwd_block (no counterpart on the pages; an
+ * implementation choice of this library).  The probabilities P_i of a query
+ * tile are kept in tensor memory over the columns of the score tile S_i that
+ * produced them, so the next S_i = Q_i K^T must not start before
+ * O_i += P_i V has read them.  The PTX ISA orders two tcgen05.mma of one
+ * thread only when they share the accumulator; it orders completion as seen
+ * through tcgen05.commit and an mbarrier wait.
+ *   order 0 (default): per key/value step, both query tiles' PV products are
+ *     issued, then each tile's next S once the commit of its PV has arrived.
+ *     Every rewrite of P's columns is ordered by commit and wait, and the
+ *     wait for one tile overlaps the other tile's PV on the tensor pipe.
+ *   order 1: per tile in turn, PV, wait for its commit, next S (the pipe
+ *     drains once per tile).
+ *   order 2: per tile in turn, PV and the next S back to back with no wait,
+ *     relying on the tensor pipe executing one thread's MMAs in issue order,
+ *     which no document states.  For measurement and tests only.
+ * All three compute the same arithmetic; the test-suite checks that their
+ * outputs are bit-identical.  Other values select order 0.  Applies to
+ * launches made after the call.
  */
-void ra_set_mma_order(int strict);
+void ra_set_mma_order(int order);
 
 /*
  * How ra_fwd and ra_fwd_block group query tiles into work items (no
@@ -263,10 +298,14 @@ void ra_set_mma_order(int strict);
 void ra_set_item_pairing(int policy);
 
 /* Drop cached tensor maps and device queries and reset the debug and policy
- * settings (no device memory is held).  Each kernel's launch attributes are
- * set once per device and then reused, which also lets ra_fwd, ra_fwd_block
- * and ra_bwd be recorded into CUDA graphs; after a device reset
- * (cudaDeviceReset), call ra_shutdown so that they are set again. */
+ * settings.  The library's device arrays (status word, work-item counters,
+ * the static scratch of ra_bwd_static) are file-scope device variables: they
+ * stay allocated while the library is loaded, and ra_shutdown leaves them and
+ * the counter sequences as they are, so launches still in flight are not
+ * disturbed.  Each kernel's launch attributes are set once per device and
+ * then reused, which also lets ra_fwd, ra_fwd_block and ra_bwd be recorded
+ * into CUDA graphs; after a device reset (cudaDeviceReset), call ra_shutdown
+ * so that they are set again. */
 void ra_shutdown(void);
 
 #ifdef __cplusplus

@@ -20,9 +20,9 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+__all__ = ["ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_measure_ceilings", "ra_get_last_device_status", "ra_status_string",
            "ra_debug_set_fault", "ra_set_mma_order", "ra_set_item_pairing", "ra_shutdown", "ra_version",
-           "RaError", "library_path",
+           "RaError", "library_path", "MMA_ORDER_GROUPED", "MMA_ORDER_STRICT", "MMA_ORDER_INORDER",
            "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT"]
 
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = 0, 1, 2, 3, 4
@@ -31,7 +31,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libringattn.so")
 _lib = None
 
-EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_get_last_device_status", "ra_status_string",
+EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_measure_ceilings", "ra_get_last_device_status", "ra_status_string",
            "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_set_mma_order",
            "ra_set_item_pairing", "ra_shutdown")
 
@@ -70,6 +70,8 @@ def _load():
     lib.ra_bwd_static.restype = i
     lib.ra_merge_partials.argtypes = [vp, i, vp, i, vp, vp, i, i, i, i, vp]
     lib.ra_merge_partials.restype = i
+    lib.ra_measure_ceilings.argtypes = [ctypes.POINTER(ctypes.c_double)]
+    lib.ra_measure_ceilings.restype = i
     lib.ra_get_last_device_status.argtypes = [vp]
     lib.ra_get_last_device_status.restype = i
     lib.ra_status_string.argtypes = [i]
@@ -312,6 +314,21 @@ def ra_merge_partials(o_parts, lse_parts, *, out=None, lse=None, want_lse: bool 
     return out, lse
 
 
+def ra_measure_ceilings(device=None) -> dict:
+    """ex2 (MUFU) and fp32 FMA rates of a device, measured by the library's
+    microbenchmark kernels (see include/ringattn.h)."""
+    import torch
+
+    lib = _load()
+    out = (ctypes.c_double * 8)()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib.ra_measure_ceilings(out), "ra_measure_ceilings")
+    keys = ("ex2_per_sm_clk", "ex2_per_s", "ffma_lanes_per_sm_clk", "ffma_lanes_per_s",
+            "ffma2_lanes_per_sm_clk", "ffma2_lanes_per_s", "sm_mhz", "sms")
+    return dict(zip(keys, list(out)))
+
+
 def ra_get_last_device_status(stream=None) -> int:
     """Synchronise ``stream``, read and clear the device status word; returns
     the status code (``RA_OK`` or ``RA_ERR_TIMEOUT`` or ``RA_ERR_CUDA``)."""
@@ -322,10 +339,14 @@ def ra_debug_set_fault(timeout_ns: int, skip_value_load: bool) -> None:
     _load().ra_debug_set_fault(int(timeout_ns), int(bool(skip_value_load)))
 
 
-def ra_set_mma_order(strict: bool) -> None:
-    """Strict (wait for each PV before rewriting S) or default in-order MMA
-    issue for subsequent ra_fwd launches; see include/ringattn.h."""
-    _load().ra_set_mma_order(int(bool(strict)))
+MMA_ORDER_GROUPED, MMA_ORDER_STRICT, MMA_ORDER_INORDER = 0, 1, 2
+
+
+def ra_set_mma_order(order: int) -> None:
+    """MMA issue order of subsequent ra_fwd / ra_fwd_block launches:
+    0 grouped (default), 1 strict alternation, 2 in-order without waits (for
+    measurement only); see include/ringattn.h."""
+    _load().ra_set_mma_order(int(order))
 
 
 def ra_set_item_pairing(policy: int) -> None:

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libringattn.so")
-SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_merge.cu"]
+SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_merge.cu", "ra_ceil.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -32,7 +32,7 @@ std::atomic<unsigned> g_prep_epoch{0};
 namespace {
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 int g_skip_value_load = 0;
-int g_strict_mma_order = 0;
+int g_mma_order = 0;  // ra::MmaOrder
 int g_item_pairing = 0;  // 0 automatic, 1 always pair when the shape allows, 2 never pair
 
 // per-device facts, queried once
@@ -43,16 +43,26 @@ struct DeviceInfo {
   unsigned int* status = nullptr;
   float* bwd_scratch = nullptr;  // the static scratch of ra_bwd_static on this device
   unsigned int* item_ctr = nullptr;  // the forward's work-item counter slots on this device
-  unsigned int launches = 0;         // forward launches so far (picks the counter slot)
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 
-ra_status device_info(DeviceInfo** out) {
+// Which counter slot the next forward launch on a device takes.  Kept apart
+// from DeviceInfo so that ra_shutdown does not restart the cycle: a launch
+// still in flight after ra_shutdown keeps its slot to itself, and captured
+// slots are never reused in this process.
+struct SlotCursor {
+  unsigned int eager = 0;     // eager launches so far (cycles through kEagerCounterSlots)
+  unsigned int captured = 0;  // captured launches so far (each keeps its slot)
+};
+SlotCursor g_slots[kMaxDevices];
+
+ra_status device_info(DeviceInfo** out, int* ordinal = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+  if (ordinal) *ordinal = dev;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceInfo& d = g_dev[dev];
   if (!d.valid) {
@@ -167,9 +177,15 @@ ra_status launch_attention(const void* q, const void* k, const void* v, void* ou
                            int B, int H, int Hkv, int Sq, int Sk, int D, int P, int causal,
                            float scale, int block, int q_tile0, int k_tile0, void* stream) {
   DeviceInfo* dev = nullptr;
-  ra_status st = device_info(&dev);
+  int ordinal = 0;
+  ra_status st = device_info(&dev, &ordinal);
   if (st != RA_OK) return st;
   if (!dev->sm103) return RA_ERR_UNSUPPORTED;
+  // a launch being recorded into a CUDA graph gets a counter slot of its own
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &capture);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  const bool captured = capture != cudaStreamCaptureStatusNone;
 
   CUtensorMap tq, tk, tv;
   if ((st = tensor_map(q, (long long)B * Sq, H, D, &tq)) != RA_OK) return st;
@@ -217,10 +233,20 @@ ra_status launch_attention(const void* q, const void* k, const void* v, void* ou
     std::lock_guard<std::mutex> lock(g_mu);
     a.timeout_ns = g_timeout_ns;
     a.skip_value_load = g_skip_value_load;
-    a.strict_mma_order = g_strict_mma_order;
+    a.mma_order = g_mma_order;
     pairing = g_item_pairing;
-    // each launch takes the next counter slot; the kernel leaves it at zero
-    a.item_ctr = dev->item_ctr + 2 * (dev->launches++ % ra::kItemCounterSlots);
+    // each eager launch takes the next of the eager slots (the kernel leaves
+    // it at zero); a captured launch takes a captured slot that no other
+    // launch will ever get
+    SlotCursor& cur = g_slots[ordinal];
+    int slot;
+    if (captured) {
+      if (cur.captured >= (unsigned)ra::kCapturedCounterSlots) return RA_ERR_UNSUPPORTED;
+      slot = ra::kEagerCounterSlots + (int)cur.captured++;
+    } else {
+      slot = (int)(cur.eager++ % (unsigned)ra::kEagerCounterSlots);
+    }
+    a.item_ctr = dev->item_ctr + 2 * slot;
   }
   // With fewer paired items than SMs the heaviest pair is the critical path:
   // one query tile per item halves it and fills the SMs better.
@@ -293,12 +319,8 @@ ra_status ra_merge_partials(const void* o_parts, int o_is_fp32, const float* lse
   if (!dev->sm103) return RA_ERR_UNSUPPORTED;
   const long long rows = (long long)B * S * H;
   if (rows >= (1ll << 31)) return RA_ERR_UNSUPPORTED;
-  const long long units = rows * (D / 8);
-  long long grid = (units + 255) / 256;
-  const long long cap = (long long)dev->sms * 8;  // 8 resident 256-thread blocks per SM
-  if (grid > cap) grid = cap;
-  cudaError_t e = ra::launch_merge(o_parts, o_is_fp32, lse_parts, n, out, lse, rows, H, S, D,
-                                   (int)grid, static_cast<cudaStream_t>(stream));
+  cudaError_t e = ra::launch_merge(o_parts, o_is_fp32, lse_parts, n, out, lse, B, H, S, D,
+                                   dev->sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return RA_OK;
 }
@@ -419,6 +441,16 @@ ra_status ra_bwd_static(const void* q, const void* k, const void* v, const void*
                          D, P, causal, scale, stream);
 }
 
+ra_status ra_measure_ceilings(double* out) {
+  if (!out) return RA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  if (!dev->sm103) return RA_ERR_UNSUPPORTED;
+  const cudaError_t e = ra::measure_ceilings(dev->sms, out);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e);
+}
+
 ra_status ra_get_last_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -450,9 +482,11 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load) {
   g_skip_value_load = skip_value_load ? 1 : 0;
 }
 
-void ra_set_mma_order(int strict) {
+void ra_set_mma_order(int order) {
   std::lock_guard<std::mutex> lock(g_mu);
-  g_strict_mma_order = strict ? 1 : 0;
+  g_mma_order = (order == ra::MMA_ORDER_STRICT || order == ra::MMA_ORDER_INORDER)
+                    ? order
+                    : ra::MMA_ORDER_GROUPED;
 }
 
 void ra_set_item_pairing(int policy) {
@@ -467,7 +501,7 @@ void ra_shutdown(void) {
   for (auto& d : g_dev) d = DeviceInfo{};
   g_timeout_ns = kDefaultTimeoutNs;
   g_skip_value_load = 0;
-  g_strict_mma_order = 0;
+  g_mma_order = 0;
   g_item_pairing = 0;
 }
 

@@ -365,15 +365,25 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 }
 
 // ---------------------------------------------------------------- MMA issuer
-// Issue order per key/value step u, for each query slot in turn:
-//   O_i += P_i(u) V(u)          once the softmax has written P_i(u)
-//   S_i(u+1) = Q_i K(u+1)^T     right behind it
-// so each slot's chain (softmax -> PV -> next S) runs independently of the
-// other slot's softmax, and the tensor pipe alternates between the two.
-// S_i(u+1) overwrites the columns that hold P_i(u), which the PV just issued
-// reads.  The default order relies on the tensor pipe executing this thread's
-// MMAs in issue order; the strict order (FwdArgs::strict_mma_order) waits for
-// the PV to complete first, which drains the pipe once per tile.
+// P_i(u) is written over the first columns of S_i, so S_i(u+1) = Q_i K(u+1)^T
+// must not start before O_i += P_i(u) V(u) has read them.  The PTX ISA orders
+// two tcgen05.mma of one thread only when they share the accumulator (and
+// shape); these two do not.  What it does order is completion as observed
+// through tcgen05.commit: the commit's mbarrier arrive happens once every
+// tcgen05 operation the thread issued before it has completed.  So the issue
+// orders below are:
+//   MMA_ORDER_GROUPED (default): per key/value step u, both slots' products
+//     O_0 += P_0(u) V(u) and O_1 += P_1(u) V(u) (each committed to its O_FREE
+//     barrier), then for each slot a wait for that commit before
+//     S_i(u+1) = Q_i K(u+1)^T.  The wait for slot 0 overlaps slot 1's PV on the
+//     tensor pipe, so the pipe does not drain; the ordering of every rewrite of
+//     P's columns is the commit/wait one.  The two slots' softmax warps run in
+//     phase.
+//   MMA_ORDER_STRICT: per slot in turn PV, wait for its commit, next S (the
+//     slots alternate; the pipe drains once per tile).
+//   MMA_ORDER_INORDER: per slot in turn PV and the next S right behind it,
+//     relying on the tensor pipe executing one thread's MMAs in issue order,
+//     which no document states; kept only to measure against.
 // A tcgen05.mma issue blocks for about the MMA's own execution time, so the
 // issuing thread keeps the work between consecutive MMAs to a few integer
 // operations: descriptors are precomputed halves plus immediate offsets, and
@@ -399,7 +409,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo
               (accumulate || kk > 0) ? 1u : 0u);
 }
 
-template <int D>
+template <int D, int ORDER>
 __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
                          volatile int* abort_flag) {
   using L = Layout<D>;
@@ -475,40 +485,76 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (!wait_bounded(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
       if (more &&
           !wait_bounded(bar(L::K_FULL + st1), ((c + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
-      // slot 0: PV(u), then S(u+1)
-      if (n0) {
-        if (!wait_bounded(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
-        tc_fence_after();
-        issue_pv<D>(tO0, tS0, v_desc(st), !first0);
-        mma_commit(bar(L::O_FREE + 0));
-        first0 = false;
+      if (ORDER == MMA_ORDER_GROUPED) {
+        // both PV products, then each slot's next S once its PV has completed
+        if (n0) {
+          if (!wait_bounded(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv<D>(tO0, tS0, v_desc(st), !first0);
+          mma_commit(bar(L::O_FREE + 0));
+          first0 = false;
+        }
+        if (n1) {
+          if (!wait_bounded(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv<D>(tO1, tS1, v_desc(st), !first1);
+          mma_commit(bar(L::O_FREE + 1));
+          first1 = false;
+        }
+        mma_commit(bar(L::V_EMPTY + st));
+        if (m0) {
+          // the PV just issued for slot 0 (the O_FREE commit of S tile s_cnt0)
+          if (!wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          tc_fence_after();
+          issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
+          mma_commit(bar(L::S_FULL + 0));
+          ++s_cnt0;
+        }
+        if (m1) {
+          if (s_cnt1 > 0 &&
+              !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          tc_fence_after();
+          issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);
+          mma_commit(bar(L::S_FULL + 1));
+          ++s_cnt1;
+        }
+        if (more) mma_commit(bar(L::K_EMPTY + st1));
+      } else {
+        // slot 0: PV(u), then S(u+1)
+        if (n0) {
+          if (!wait_bounded(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv<D>(tO0, tS0, v_desc(st), !first0);
+          mma_commit(bar(L::O_FREE + 0));
+          first0 = false;
+        }
+        if (m0) {
+          if (ORDER == MMA_ORDER_STRICT &&
+              !wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          tc_fence_after();
+          issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
+          mma_commit(bar(L::S_FULL + 0));
+          ++s_cnt0;
+        }
+        // slot 1: PV(u), then S(u+1)
+        if (n1) {
+          if (!wait_bounded(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv<D>(tO1, tS1, v_desc(st), !first1);
+          mma_commit(bar(L::O_FREE + 1));
+          first1 = false;
+        }
+        if (m1) {
+          if (ORDER == MMA_ORDER_STRICT && s_cnt1 > 0 &&
+              !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          tc_fence_after();
+          issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);
+          mma_commit(bar(L::S_FULL + 1));
+          ++s_cnt1;
+        }
+        mma_commit(bar(L::V_EMPTY + st));
+        if (more) mma_commit(bar(L::K_EMPTY + st1));
       }
-      if (m0) {
-        if (a.strict_mma_order &&
-            !wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
-        tc_fence_after();
-        issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
-        mma_commit(bar(L::S_FULL + 0));
-        ++s_cnt0;
-      }
-      // slot 1: PV(u), then S(u+1)
-      if (n1) {
-        if (!wait_bounded(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
-        tc_fence_after();
-        issue_pv<D>(tO1, tS1, v_desc(st), !first1);
-        mma_commit(bar(L::O_FREE + 1));
-        first1 = false;
-      }
-      if (m1) {
-        if (a.strict_mma_order && s_cnt1 > 0 &&
-            !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
-        tc_fence_after();
-        issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);
-        mma_commit(bar(L::S_FULL + 1));
-        ++s_cnt1;
-      }
-      mma_commit(bar(L::V_EMPTY + st));
-      if (more) mma_commit(bar(L::K_EMPTY + st1));
       if (u + 2 == ns) {  // the item's last S MMAs are issued: its Q tiles may be replaced
         mma_commit(bar(L::Q_EMPTY + 0));
         if (it.valid1) mma_commit(bar(L::Q_EMPTY + 1));
@@ -871,7 +917,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpTma) {
       if ((threadIdx.x & 31) == 0) tma_role<D>(&tm_q, &tm_k, &tm_v, a, sbase, abort_flag);
     } else if (warp == kWarpMma) {
-      if ((threadIdx.x & 31) == 0) mma_role<D>(a, sbase, tmem, abort_flag);
+      if ((threadIdx.x & 31) == 0) {
+        if (a.mma_order == MMA_ORDER_STRICT)
+          mma_role<D, MMA_ORDER_STRICT>(a, sbase, tmem, abort_flag);
+        else if (a.mma_order == MMA_ORDER_INORDER)
+          mma_role<D, MMA_ORDER_INORDER>(a, sbase, tmem, abort_flag);
+        else
+          mma_role<D, MMA_ORDER_GROUPED>(a, sbase, tmem, abort_flag);
+      }
     }
   }
 

@@ -16,6 +16,13 @@ enum PairMode : int {
   MODE_QTILES = 2,  // two consecutive 128-row tiles of one head, same chunk
 };
 
+// Issue order of the forward's MMA thread (see ra_fwd.cu, "MMA issuer").
+enum MmaOrder : int {
+  MMA_ORDER_GROUPED = 0,  // both slots' PV, then each next S after its PV's commit (default)
+  MMA_ORDER_STRICT = 1,   // per slot: PV, wait for its commit, next S
+  MMA_ORDER_INORDER = 2,  // per slot: PV and next S back to back (relies on in-order execution)
+};
+
 // Kernel arguments besides the three tensor maps (q, k, v).
 struct FwdArgs {
   void* out;             // bf16 [B,S,H,D]
@@ -37,7 +44,7 @@ struct FwdArgs {
   float scale_log2;      // scale * log2(e)
   unsigned long long timeout_ns;
   int skip_value_load;   // failure-path test hook
-  int strict_mma_order;  // 1: wait for O_i += P_i V to complete before S_i is rewritten
+  int mma_order;         // MmaOrder: how S_i(u+1) is ordered after O_i += P_i(u) V
   unsigned int* item_ctr;  // this launch's work-item counter pair (next item, CTAs done), zero at launch
 };
 
@@ -102,9 +109,14 @@ inline cudaError_t prepare_kernel(Kernel kernel, int regs, int smem,
   if (cache) prepared[dev].store(mark, std::memory_order_release);
   return cudaSuccess;
 }
-// Work-item counter slots of the forward (2 words each); a launch takes the
-// next slot in turn, so up to this many launches may run at once.
-constexpr int kItemCounterSlots = 64;
+// Work-item counter slots of the forward (2 words each).  Eager launches take
+// the first kEagerCounterSlots in turn, so up to that many may run at once.  A
+// launch recorded into a CUDA graph keeps its slot for every replay, so it
+// takes one of the remaining slots, which is never handed out again in this
+// process: no eager launch and no other captured launch can share it.
+constexpr int kEagerCounterSlots = 64;
+constexpr int kCapturedCounterSlots = 4032;
+constexpr int kItemCounterSlots = kEagerCounterSlots + kCapturedCounterSlots;
 cudaError_t item_counter_ptr(unsigned int** p);
 cudaError_t read_and_clear_status(unsigned int* value);
 
@@ -119,9 +131,12 @@ cudaError_t launch_bwd_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
                           int grid, cudaStream_t stream);
 
+// ra_ceil.cu: ex2 and fp32 FMA rates of this device (see ra_measure_ceilings)
+cudaError_t measure_ceilings(int sms, double* out);
+
 // ra_merge.cu
 cudaError_t launch_merge(const void* o_parts, int o_is_fp32, const float* lse_parts, int n,
-                         void* out, float* lse, long long rows, int H, int S, int D, int grid,
+                         void* out, float* lse, int B, int H, int S, int D, int sms,
                          cudaStream_t stream);
 
 }  // namespace ra

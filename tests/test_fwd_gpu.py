@@ -283,6 +283,51 @@ def test_cuda_graph_capture_and_replay(ralib, cuda_ok):
     assert ralib.ra_get_last_device_status() == ralib.RA_OK
 
 
+def test_graph_replays_beside_many_eager_launches(ralib, cuda_ok):
+    """A launch recorded into a CUDA graph keeps one work-item counter for every
+    replay, one that eager launches never take.  Replays on one stream while
+    more than 64 eager launches run on another (so the eager launches cycle
+    through all their counters at least once during the replays) must each
+    reproduce the sequential result bit for bit."""
+    w = _claiming_workload()
+    ins_g = tuple(t.cuda() for t in make_inputs(w, seed=79))
+    ins_e = tuple(t.cuda() for t in make_inputs(w, seed=83))
+    ref_g = ralib.ra_fwd(*ins_g, P=w.P, causal=True)
+    ref_e = ralib.ra_fwd(*ins_e, P=w.P, causal=True)
+    out_g, lse_g = torch.empty_like(ref_g[0]), torch.empty_like(ref_g[1])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ralib.ra_fwd(*ins_g, P=w.P, causal=True, out=out_g, lse=lse_g)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ralib.ra_fwd(*ins_g, P=w.P, causal=True, out=out_g, lse=lse_g)
+    torch.cuda.synchronize()
+    n_eager, n_replay = 70, 24
+    outs_e = [(torch.zeros_like(ref_e[0]), torch.zeros_like(ref_e[1])) for _ in range(n_eager)]
+    snaps = [(torch.empty_like(ref_g[0]), torch.empty_like(ref_g[1])) for _ in range(n_replay)]
+    s_g, s_e = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s_g):
+        for so, sl in snaps:
+            out_g.zero_()
+            lse_g.zero_()
+            g.replay()
+            so.copy_(out_g)
+            sl.copy_(lse_g)
+    with torch.cuda.stream(s_e):
+        for o, l in outs_e:
+            ralib.ra_fwd(*ins_e, P=w.P, causal=True, out=o, lse=l, stream=s_e)
+    torch.cuda.synchronize()
+    assert ralib.ra_get_last_device_status() == ralib.RA_OK
+    for so, sl in snaps:
+        assert torch.equal(so, ref_g[0]) and torch.equal(sl, ref_g[1])
+    for o, l in outs_e:
+        assert torch.equal(o, ref_e[0]) and torch.equal(l, ref_e[1])
+
+
 def test_launches_after_shutdown(ralib, cuda_ok):
     """ra_shutdown drops the host caches and starts a new kernel-preparation
     epoch; the next launches prepare again and give the same result."""
@@ -335,26 +380,31 @@ def test_stream_argument_is_used(ralib, cuda_ok, oracle_mod):
     assert_parity(compare(out, lse, o_ref, l_ref), "side stream")
 
 
-@pytest.mark.parametrize("name", ["gqa_s16384", "d64_s32768", "small"])
-def test_default_mma_order_is_bit_identical_to_strict_order(ralib, cuda_ok, name):
-    """The default issue order puts the next S MMA right behind the PV MMA
-    that reads the columns it overwrites (relying on in-order execution of one
-    thread's MMAs); the strict order waits for the PV to complete first.  Same
-    arithmetic, so any reordering hazard would show up as a difference."""
+@pytest.mark.parametrize("name", ["tiny", "causal_s4096", "gqa_s16384", "long_s65536",
+                                  "d64_s32768", "small"])
+def test_mma_orders_are_bit_identical(ralib, cuda_ok, name):
+    """The three MMA issue orders run the same arithmetic in the same
+    accumulation order; they differ only in when the next S product of a query
+    tile is issued relative to the PV product that reads the columns it
+    rewrites.  Any ordering hazard would corrupt P and show up as a
+    difference.  Every workload, with paired query tiles forced (the pairs are
+    where the orders differ), and the default pairing for the default order."""
     w = WORKLOADS[name] if name in WORKLOADS else Workload("small", 2, 8, 2, 2048, 128, 4, True)
     q, k, v = make_inputs(w, seed=43)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     outs = []
-    ralib.ra_set_item_pairing(1)  # the paired chains are the ones the order matters for
+    ralib.ra_set_item_pairing(1)
     try:
-        for strict in (True, False, False):
-            ralib.ra_set_mma_order(strict)
+        for order in (ralib.MMA_ORDER_STRICT, ralib.MMA_ORDER_GROUPED, ralib.MMA_ORDER_INORDER,
+                      ralib.MMA_ORDER_GROUPED):
+            ralib.ra_set_mma_order(order)
             o, l = ralib.ra_fwd(qd, kd, vd, P=w.P, causal=w.causal)
             torch.cuda.synchronize()
             assert ralib.ra_get_last_device_status() == 0
             outs.append((o, l))
+            del o, l
     finally:
-        ralib.ra_set_mma_order(False)
+        ralib.ra_set_mma_order(ralib.MMA_ORDER_GROUPED)
         ralib.ra_set_item_pairing(0)
     for o, l in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])

@@ -20,7 +20,12 @@ def _partials(n, B, S, H, D, seed, empty_frac=0.1, all_empty_rows=3):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("shape", [(1, 1, 128, 1, 64), (3, 2, 96, 4, 128), (8, 1, 200, 3, 64)])
+@pytest.mark.parametrize("shape", [
+    (1, 1, 128, 1, 64), (3, 2, 96, 4, 128), (8, 1, 200, 3, 64),
+    (33, 2, 37, 5, 64),    # many partials: short position tiles, a ragged last tile
+    (8, 1, 1000, 32, 8),   # one 16-byte vector per row
+    (2, 1, 3, 4500, 8),    # n*H past the shared-memory tile budget: the per-row kernel
+])
 def test_merge_parity(ralib, cuda_ok, oracle_mod, dtype, shape):
     n, B, S, H, D = shape
     o, lse = _partials(n, B, S, H, D, seed=sum(shape))

@@ -53,3 +53,22 @@ def test_static_scratch_matches_workspace_entry_on_consecutive_calls(ralib, cuda
     for q, k, v, out, lse, do, ref, got in cases:
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
+
+
+@pytest.mark.gpu
+def test_static_scratch_at_its_largest_accepted_size(ralib, cuda_ok):
+    """B*H*S == 2^21 rows exactly: the second half of the scratch (-delta) then
+    ends at the last byte of the array.  The result must equal ra_bwd's with a
+    workspace bit for bit."""
+    w = Workload("noalloc_max", 1, 32, 8, 65536, 64, 16, True)
+    assert w.B * w.H * w.S == MAX_ROWS
+    q, k, v = (t.cuda() for t in make_inputs(w, seed=44))
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(144)).bfloat16().cuda()
+    out, lse = ralib.ra_fwd(q, k, v, P=w.P, causal=True)
+    ref = ralib.ra_bwd(q, k, v, out, lse, do, P=w.P, causal=True)
+    got = tuple(torch.empty_like(t) for t in (q, k, v))
+    ralib.ra_bwd_static(q, k, v, out, lse, do, *got, P=w.P, causal=True)
+    torch.cuda.synchronize()
+    assert ralib.ra_get_last_device_status() == 0
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
