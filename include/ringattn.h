@@ -269,12 +269,12 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
  * O_i += P_i V has read them.  The PTX ISA orders two tcgen05.mma of one
  * thread only when they share the accumulator; it orders completion as seen
  * through tcgen05.commit and an mbarrier wait.
- *   order 0 (default): per key/value step, both query tiles' PV products are
- *     issued, then each tile's next S once the commit of its PV has arrived.
- *     Every rewrite of P's columns is ordered by commit and wait, and the
- *     wait for one tile overlaps the other tile's PV on the tensor pipe.
- *   order 1: per tile in turn, PV, wait for its commit, next S (the pipe
- *     drains once per tile).
+ *   order 0 (default): per key/value step and query tile in turn, PV, a wait
+ *     for its commit, the next S.  Every rewrite of P's columns is ordered by
+ *     commit and wait; the tensor pipe drains once per tile.
+ *   order 1: per key/value step, both query tiles' PV products, then each
+ *     tile's next S once the commit of its PV has arrived (no drain, but the
+ *     two tiles' softmax work runs at the same time and competes; slower).
  *   order 2: per tile in turn, PV and the next S back to back with no wait,
  *     relying on the tensor pipe executing one thread's MMAs in issue order,
  *     which no document states.  For measurement and tests only.

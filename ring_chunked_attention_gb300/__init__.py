@@ -339,13 +339,13 @@ def ra_debug_set_fault(timeout_ns: int, skip_value_load: bool) -> None:
     _load().ra_debug_set_fault(int(timeout_ns), int(bool(skip_value_load)))
 
 
-MMA_ORDER_GROUPED, MMA_ORDER_STRICT, MMA_ORDER_INORDER = 0, 1, 2
+MMA_ORDER_STRICT, MMA_ORDER_GROUPED, MMA_ORDER_INORDER = 0, 1, 2
 
 
 def ra_set_mma_order(order: int) -> None:
     """MMA issue order of subsequent ra_fwd / ra_fwd_block launches:
-    0 grouped (default), 1 strict alternation, 2 in-order without waits (for
-    measurement only); see include/ringattn.h."""
+    0 strict (default), 1 grouped, 2 in-order without waits (for measurement
+    only); see include/ringattn.h."""
     _load().ra_set_mma_order(int(order))
 
 

@@ -484,9 +484,9 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load) {
 
 void ra_set_mma_order(int order) {
   std::lock_guard<std::mutex> lock(g_mu);
-  g_mma_order = (order == ra::MMA_ORDER_STRICT || order == ra::MMA_ORDER_INORDER)
+  g_mma_order = (order == ra::MMA_ORDER_GROUPED || order == ra::MMA_ORDER_INORDER)
                     ? order
-                    : ra::MMA_ORDER_GROUPED;
+                    : ra::MMA_ORDER_STRICT;
 }
 
 void ra_set_item_pairing(int policy) {

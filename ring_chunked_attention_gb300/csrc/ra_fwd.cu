@@ -15,7 +15,9 @@
 //   warp  8    producer (one thread): claims the CTA's next work item at run
 //              time and hands its id on, then TMA-loads the Q tiles and the
 //              K/V tiles into an NS-stage ring
-//   warp  9    MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V
+//   warp  9    MMA issuer (the whole warp runs the loop and waits; one
+//              elected lane issues each tcgen05.mma and commit):
+//              S_i = Q_i K^T and O_i += P_i V
 //   warps 10-11 idle (they complete the producer warpgroup)
 // Registers are split with setmaxnreg: the launch gives every thread 168
 // (three warps per SM sub-partition); the two softmax warpgroups raise theirs
@@ -96,7 +98,11 @@ struct Layout {
   static constexpr int V_OFF = K_OFF + NS * TILE;
   // row-sum columns of the PV MMA (D = 64): one 64-column block of bf16 ones
   static constexpr bool kRowSum = SoftmaxPolicy<D>::kMmaRowSum;
-  static constexpr int ONES_OFF = V_OFF + NS * TILE;
+  // D = 128: per softmax warp a 4 KiB block that turns the warp's 32 output
+  // rows (one 64-column half at a time) into whole 128-byte lines per store
+  static constexpr bool kLineStores = (D == 128);
+  static constexpr int EPI_OFF = V_OFF + NS * TILE;
+  static constexpr int ONES_OFF = EPI_OFF + (kLineStores ? 8 * 4096 : 0);
   static constexpr int OW = kRowSum ? D + 16 : D;  // O columns per slot
   static constexpr int BAR_OFF = ONES_OFF + (kRowSum ? BLOCK : 0);
   // barrier indices
@@ -370,24 +376,32 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 // two tcgen05.mma of one thread only when they share the accumulator (and
 // shape); these two do not.  What it does order is completion as observed
 // through tcgen05.commit: the commit's mbarrier arrive happens once every
-// tcgen05 operation the thread issued before it has completed.  So the issue
-// orders below are:
-//   MMA_ORDER_GROUPED (default): per key/value step u, both slots' products
-//     O_0 += P_0(u) V(u) and O_1 += P_1(u) V(u) (each committed to its O_FREE
-//     barrier), then for each slot a wait for that commit before
-//     S_i(u+1) = Q_i K(u+1)^T.  The wait for slot 0 overlaps slot 1's PV on the
-//     tensor pipe, so the pipe does not drain; the ordering of every rewrite of
-//     P's columns is the commit/wait one.  The two slots' softmax warps run in
-//     phase.
-//   MMA_ORDER_STRICT: per slot in turn PV, wait for its commit, next S (the
-//     slots alternate; the pipe drains once per tile).
-//   MMA_ORDER_INORDER: per slot in turn PV and the next S right behind it,
+// tcgen05 operation the thread issued before it has completed.  The issue
+// orders:
+//   MMA_ORDER_STRICT (default): per key/value step u, for each slot in turn:
+//     O_i += P_i(u) V(u), committed to the slot's O_FREE barrier; a wait for
+//     that commit; S_i(u+1) = Q_i K(u+1)^T.  Every rewrite of P's columns is
+//     ordered by commit and wait; the tensor pipe drains once per tile (the
+//     last PV MMA's execution plus the commit's round trip).
+//   MMA_ORDER_GROUPED: both slots' PV products, then each slot's S after the
+//     commit of its PV.  The wait for slot 0 overlaps slot 1's PV, so the pipe
+//     does not drain, but the two slots' softmax warps run in phase and compete
+//     for the same issue slots: measured 17 % slower than the default on the
+//     GQA workload.
+//   MMA_ORDER_INORDER: per slot, PV and the next S back to back with no wait,
 //     relying on the tensor pipe executing one thread's MMAs in issue order,
-//     which no document states; kept only to measure against.
-// A tcgen05.mma issue blocks for about the MMA's own execution time, so the
-// issuing thread keeps the work between consecutive MMAs to a few integer
-// operations: descriptors are precomputed halves plus immediate offsets, and
-// the step sequence comes from a division-free cursor.
+//     which no document states; kept only to measure against (4.5 % faster
+//     than the default on the GQA workload).
+// The whole MMA warp runs the loop: every wait is taken by all 32 lanes
+// (a vote makes its outcome warp-uniform), and each tcgen05.mma and
+// tcgen05.commit is issued by the one lane elect.sync picks.  Measured against
+// a loop run by a single lane (GQA workload, strict order): 3.43 against
+// 3.48 ms, and 23.2 against 24.8 ms on the D = 64 workload, bit-identical
+// outputs.  Back-to-back MMAs run at the pipe's rate however their operands
+// are formed (a microbenchmark: 64 cycles per M128 N128 K16 MMA), so the time
+// between MMA groups (waits, commits) is what the loop keeps short:
+// descriptors are precomputed halves plus immediate offsets, and the step
+// sequence comes from a division-free cursor.
 
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {
@@ -396,7 +410,7 @@ __device__ __forceinline__ void issue_s(uint32_t tS, uint32_t q_lo, uint32_t k_l
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (uint32_t)((kk >> 2) * L::BLOCK + (kk & 3) * 32) >> 4;
-    mma_ss_lh(tS, q_lo + off, kDescHiSw128, k_lo + off, kDescHiSw128, idesc_s, kk > 0 ? 1u : 0u);
+    mma_ss_lh_e(tS, q_lo + off, kDescHiSw128, k_lo + off, kDescHiSw128, idesc_s, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -405,8 +419,17 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo
   constexpr uint32_t idesc_pv = make_idesc(kBM, Layout<D>::OW, 1);
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk)
-    mma_ts_lh(tO, tP + kk * 8, v_lo + (uint32_t)(kk * (2048 >> 4)), kDescHiSw128, idesc_pv,
+    mma_ts_lh_e(tO, tP + kk * 8, v_lo + (uint32_t)(kk * (2048 >> 4)), kDescHiSw128, idesc_pv,
               (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Bounded wait taken by all 32 lanes of a warp; the vote makes the outcome
+// (and so the branch that follows) warp-uniform.
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         const FwdArgs& a) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const bool ok = wait_slow(bar, parity, abort_flag, a.timeout_ns, a.status);
+  return __all_sync(0xffffffffu, ok);
 }
 
 template <int D, int ORDER>
@@ -434,14 +457,14 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
 
   while (ok) {
     // the next item with work: its id comes with its first query tile (-1: none left)
-    if (!wait_bounded(bar(L::Q_FULL + 0), q_cnt0 & 1, abort_flag, a)) break;
+    if (!wait_all(bar(L::Q_FULL + 0), q_cnt0 & 1, abort_flag, a)) break;
     ++q_cnt0;
     const int x = ld_shared_i32(sbase + L::QID_OFF);
     if (x < 0) break;
     const Item it = decode_item(a, x);
     const int ns = n_steps(a, it);
     if (it.valid1) {
-      if (!wait_bounded(bar(L::Q_FULL + 1), q_cnt1 & 1, abort_flag, a)) break;
+      if (!wait_all(bar(L::Q_FULL + 1), q_cnt1 & 1, abort_flag, a)) break;
       ++q_cnt1;
     }
     // slot i needs key tile kt iff kt <= lim_i (needs_tile's causal test,
@@ -453,25 +476,25 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     // prologue: S(0) for both slots
     {
       const int st = c % L::NS;
-      if (!wait_bounded(bar(L::K_FULL + st), (c / L::NS) & 1, abort_flag, a)) break;
+      if (!wait_all(bar(L::K_FULL + st), (c / L::NS) & 1, abort_flag, a)) break;
       if (nxt.kt <= lim0) {
-        if (s_cnt0 > 0 && !wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) break;
+        if (s_cnt0 > 0 && !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) break;
         tc_fence_after();
         issue_s<D>(tS0, q_lo0, k_lo0 + st * kStageLo);
-        mma_commit(bar(L::S_FULL + 0));
+        mma_commit_e(bar(L::S_FULL + 0));
         ++s_cnt0;
       }
       if (nxt.kt <= lim1) {
-        if (s_cnt1 > 0 && !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) break;
+        if (s_cnt1 > 0 && !wait_all(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) break;
         tc_fence_after();
         issue_s<D>(tS1, q_lo1, k_lo0 + st * kStageLo);
-        mma_commit(bar(L::S_FULL + 1));
+        mma_commit_e(bar(L::S_FULL + 1));
         ++s_cnt1;
       }
-      mma_commit(bar(L::K_EMPTY + st));
+      mma_commit_e(bar(L::K_EMPTY + st));
       if (ns == 1) {
-        mma_commit(bar(L::Q_EMPTY + 0));
-        if (it.valid1) mma_commit(bar(L::Q_EMPTY + 1));
+        mma_commit_e(bar(L::Q_EMPTY + 0));
+        if (it.valid1) mma_commit_e(bar(L::Q_EMPTY + 1));
       }
     }
     bool first0 = true, first1 = true;
@@ -482,87 +505,87 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (more) nxt.next();
       const bool m0 = more && nxt.kt <= lim0, m1 = more && nxt.kt <= lim1;
       const int st1 = (c + 1) % L::NS;
-      if (!wait_bounded(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+      if (!wait_all(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
       if (more &&
-          !wait_bounded(bar(L::K_FULL + st1), ((c + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+          !wait_all(bar(L::K_FULL + st1), ((c + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
       if (ORDER == MMA_ORDER_GROUPED) {
         // both PV products, then each slot's next S once its PV has completed
         if (n0) {
-          if (!wait_bounded(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          if (!wait_all(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_pv<D>(tO0, tS0, v_desc(st), !first0);
-          mma_commit(bar(L::O_FREE + 0));
+          mma_commit_e(bar(L::O_FREE + 0));
           first0 = false;
         }
         if (n1) {
-          if (!wait_bounded(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          if (!wait_all(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_pv<D>(tO1, tS1, v_desc(st), !first1);
-          mma_commit(bar(L::O_FREE + 1));
+          mma_commit_e(bar(L::O_FREE + 1));
           first1 = false;
         }
-        mma_commit(bar(L::V_EMPTY + st));
+        mma_commit_e(bar(L::V_EMPTY + st));
         if (m0) {
           // the PV just issued for slot 0 (the O_FREE commit of S tile s_cnt0)
-          if (!wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          if (!wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
-          mma_commit(bar(L::S_FULL + 0));
+          mma_commit_e(bar(L::S_FULL + 0));
           ++s_cnt0;
         }
         if (m1) {
           if (s_cnt1 > 0 &&
-              !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+              !wait_all(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);
-          mma_commit(bar(L::S_FULL + 1));
+          mma_commit_e(bar(L::S_FULL + 1));
           ++s_cnt1;
         }
-        if (more) mma_commit(bar(L::K_EMPTY + st1));
+        if (more) mma_commit_e(bar(L::K_EMPTY + st1));
       } else {
         // slot 0: PV(u), then S(u+1)
         if (n0) {
-          if (!wait_bounded(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          if (!wait_all(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_pv<D>(tO0, tS0, v_desc(st), !first0);
-          mma_commit(bar(L::O_FREE + 0));
+          mma_commit_e(bar(L::O_FREE + 0));
           first0 = false;
         }
         if (m0) {
           if (ORDER == MMA_ORDER_STRICT &&
-              !wait_bounded(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+              !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
-          mma_commit(bar(L::S_FULL + 0));
+          mma_commit_e(bar(L::S_FULL + 0));
           ++s_cnt0;
         }
         // slot 1: PV(u), then S(u+1)
         if (n1) {
-          if (!wait_bounded(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          if (!wait_all(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_pv<D>(tO1, tS1, v_desc(st), !first1);
-          mma_commit(bar(L::O_FREE + 1));
+          mma_commit_e(bar(L::O_FREE + 1));
           first1 = false;
         }
         if (m1) {
           if (ORDER == MMA_ORDER_STRICT && s_cnt1 > 0 &&
-              !wait_bounded(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+              !wait_all(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);
-          mma_commit(bar(L::S_FULL + 1));
+          mma_commit_e(bar(L::S_FULL + 1));
           ++s_cnt1;
         }
-        mma_commit(bar(L::V_EMPTY + st));
-        if (more) mma_commit(bar(L::K_EMPTY + st1));
+        mma_commit_e(bar(L::V_EMPTY + st));
+        if (more) mma_commit_e(bar(L::K_EMPTY + st1));
       }
       if (u + 2 == ns) {  // the item's last S MMAs are issued: its Q tiles may be replaced
-        mma_commit(bar(L::Q_EMPTY + 0));
-        if (it.valid1) mma_commit(bar(L::Q_EMPTY + 1));
+        mma_commit_e(bar(L::Q_EMPTY + 0));
+        if (it.valid1) mma_commit_e(bar(L::Q_EMPTY + 1));
       }
     }
   }
   // Every MMA this thread issued completes before tensor memory is freed.
-  mma_commit(bar(L::DONE));
+  mma_commit_e(bar(L::DONE));
   wait_drain(bar(L::DONE), 0, a.timeout_ns);
 }
 
@@ -841,20 +864,59 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           l_norm = __uint_as_float(ls[0]);
         }
         const float inv_l = 1.0f / l_norm;
-        uint4* orow = reinterpret_cast<uint4*>(
-            static_cast<__nv_bfloat16*>(a.out) + (((size_t)it.b * a.S + srow) * a.H + h) * D);
+        if constexpr (Layout<D>::kLineStores) {
+          // Each 64-column half of the warp's 32 rows goes through the warp's
+          // block: lane i writes its row's 128 bytes (16-byte chunk c at
+          // c ^ (i % 8), so a store touches every bank once per 8 lanes), then
+          // each lane reads chunk (lane % 8) of row 4 j + lane / 8 and stores
+          // it: 8 lanes cover one row's 128 contiguous bytes, a warp store 4
+          // whole lines.
+          const uint32_t blk = sbase + L::EPI_OFF + (uint32_t)warp * 4096u;
+          const int row0 = my_qt * kBM + (r & ~31);  // the warp's first row
+          __nv_bfloat16* obase = static_cast<__nv_bfloat16*>(a.out);
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + c0, o);
-          tmem_wait_ld_regs(o);
-          uint32_t w[16];
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t o[32], w[2][16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+            for (int part = 0; part < 2; ++part) {
+              tmem_ld32(tO + hh * 64 + part * 32, o);
+              tmem_wait_ld_regs(o);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            orow[c0 / 8 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+              for (int j = 0; j < 16; ++j)
+                w[part][j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l,
+                                         __uint_as_float(o[2 * j + 1]) * inv_l);
+            }
+            __syncwarp();  // the previous half has been read out of the block
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t* src = &w[c >> 2][(c & 3) * 4];
+              st_shared_v4(blk + lane * 128 + ((c ^ (lane & 7)) << 4), src[0], src[1], src[2], src[3]);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int row = 4 * j + (lane >> 3), c = lane & 7;
+              const uint4 v = ld_shared_v4(blk + row * 128 + ((c ^ (row & 7)) << 4));
+              *reinterpret_cast<uint4*>(obase + (((size_t)it.b * a.S + row0 + row) * a.H + h) * D +
+                                        hh * 64 + c * 8) = v;
+            }
+          }
+        } else {
+          uint4* orow = reinterpret_cast<uint4*>(
+              static_cast<__nv_bfloat16*>(a.out) + (((size_t)it.b * a.S + srow) * a.H + h) * D);
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + c0, o);
+            tmem_wait_ld_regs(o);
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              orow[c0 / 8 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
         }
         if (a.lse)
           a.lse[((size_t)it.b * a.H + h) * a.S + srow] =
@@ -917,13 +979,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpTma) {
       if ((threadIdx.x & 31) == 0) tma_role<D>(&tm_q, &tm_k, &tm_v, a, sbase, abort_flag);
     } else if (warp == kWarpMma) {
-      if ((threadIdx.x & 31) == 0) {
-        if (a.mma_order == MMA_ORDER_STRICT)
-          mma_role<D, MMA_ORDER_STRICT>(a, sbase, tmem, abort_flag);
+      {
+        if (a.mma_order == MMA_ORDER_GROUPED)
+          mma_role<D, MMA_ORDER_GROUPED>(a, sbase, tmem, abort_flag);
         else if (a.mma_order == MMA_ORDER_INORDER)
           mma_role<D, MMA_ORDER_INORDER>(a, sbase, tmem, abort_flag);
         else
-          mma_role<D, MMA_ORDER_GROUPED>(a, sbase, tmem, abort_flag);
+          mma_role<D, MMA_ORDER_STRICT>(a, sbase, tmem, abort_flag);
       }
     }
   }

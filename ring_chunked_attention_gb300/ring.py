@@ -355,13 +355,16 @@ def ring_attention(q, k, v, *, causal: bool, layout: str = "contiguous", scale=N
     world x the local rows)."""
     import torch.distributed as dist
 
-    world = dist.get_world_size(group)
-    rank = dist.get_rank(group)
+    if dist.is_available() and dist.is_initialized():
+        world, rank = dist.get_world_size(group), dist.get_rank(group)
+    else:  # no process group: a ring of one rank (nothing is exchanged)
+        world, rank = 1, 0
     zig = layout == "zigzag"
     B, L, H, D = tuple(q.shape[1:] if zig else q.shape)
     Hkv = k.shape[-2]
     spec = RingSpec(world, B, H, Hkv, S or world * L * (2 if zig else 1), D, causal, layout, scale)
-    return RingRank(spec, rank, q, k, v, DistTransport(group), ops).run()
+    transport = DistTransport(group) if world > 1 else None
+    return RingRank(spec, rank, q, k, v, transport, ops).run()
 
 
 def virtual_ring_attention(qs, ks, vs, *, causal: bool, layout: str = "contiguous", scale=None):

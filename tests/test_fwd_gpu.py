@@ -396,7 +396,7 @@ def test_mma_orders_are_bit_identical(ralib, cuda_ok, name):
     ralib.ra_set_item_pairing(1)
     try:
         for order in (ralib.MMA_ORDER_STRICT, ralib.MMA_ORDER_GROUPED, ralib.MMA_ORDER_INORDER,
-                      ralib.MMA_ORDER_GROUPED):
+                      ralib.MMA_ORDER_STRICT):
             ralib.ra_set_mma_order(order)
             o, l = ralib.ra_fwd(qd, kd, vd, P=w.P, causal=w.causal)
             torch.cuda.synchronize()
@@ -404,7 +404,7 @@ def test_mma_orders_are_bit_identical(ralib, cuda_ok, name):
             outs.append((o, l))
             del o, l
     finally:
-        ralib.ra_set_mma_order(ralib.MMA_ORDER_GROUPED)
+        ralib.ra_set_mma_order(ralib.MMA_ORDER_STRICT)
         ralib.ra_set_item_pairing(0)
     for o, l in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])

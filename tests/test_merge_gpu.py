@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.parity import MAX_ABS, MEAN_ABS
+from tests.parity import MAX_ABS, MEAN_ABS, assert_parity, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -34,8 +34,10 @@ def test_merge_parity(ralib, cuda_ok, oracle_mod, dtype, shape):
     torch.cuda.synchronize()
     o_ref, l_ref = oracle_mod.merge(o_in.double().numpy(), lse.double().numpy())
     got = out.double().cpu().numpy()
-    err = np.abs(got - o_ref)
-    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS
+    # out is bf16: where |out| >= 4 one half-ulp (2^-6) exceeds the max-abs gate, so
+    # an element equal to the correctly rounded oracle value passes as in the
+    # forward's parity checks (tests/parity.py)
+    assert_parity(compare(out, None, o_ref, None), f"merge {shape} {dtype}")
     lg = lse_out.double().cpu().numpy()
     fin = np.isfinite(l_ref)
     assert (np.isneginf(lg) == np.isneginf(l_ref)).all()
