@@ -100,9 +100,11 @@ struct Layout {
   static constexpr bool kRowSum = SoftmaxPolicy<D>::kMmaRowSum;
   // D = 128: per softmax warp a 4 KiB block that turns the warp's 32 output
   // rows (one 64-column half at a time) into whole 128-byte lines per store
-  static constexpr bool kLineStores = (D == 128);
+  // D = 64 rows are 128 bytes: 2 KiB per warp holds 16 of its 32 rows at a time
+  static constexpr bool kLineStores = true;
+  static constexpr int EPI_BLOCK = (D == 128) ? 4096 : 2048;
   static constexpr int EPI_OFF = V_OFF + NS * TILE;
-  static constexpr int ONES_OFF = EPI_OFF + (kLineStores ? 8 * 4096 : 0);
+  static constexpr int ONES_OFF = EPI_OFF + 8 * EPI_BLOCK;
   static constexpr int OW = kRowSum ? D + 16 : D;  // O columns per slot
   static constexpr int BAR_OFF = ONES_OFF + (kRowSum ? BLOCK : 0);
   // barrier indices
@@ -871,11 +873,44 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           // each lane reads chunk (lane % 8) of row 4 j + lane / 8 and stores
           // it: 8 lanes cover one row's 128 contiguous bytes, a warp store 4
           // whole lines.
-          const uint32_t blk = sbase + L::EPI_OFF + (uint32_t)warp * 4096u;
+          const uint32_t blk = sbase + L::EPI_OFF + (uint32_t)warp * (uint32_t)L::EPI_BLOCK;
           const int row0 = my_qt * kBM + (r & ~31);  // the warp's first row
           __nv_bfloat16* obase = static_cast<__nv_bfloat16*>(a.out);
+          if constexpr (D == 64) {
+            // one 128-byte row per lane; 16 lanes' rows at a time
+            uint32_t o[32], w[2][16];
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              tmem_ld32(tO + part * 32, o);
+              tmem_wait_ld_regs(o);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                w[part][j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l,
+                                         __uint_as_float(o[2 * j + 1]) * inv_l);
+            }
 #pragma unroll 1
-          for (int hh = 0; hh < 2; ++hh) {
+            for (int half = 0; half < 2; ++half) {
+              __syncwarp();  // the previous round has been read out of the block
+              if ((lane >> 4) == half) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const uint32_t* src = &w[c >> 2][(c & 3) * 4];
+                  st_shared_v4(blk + (lane & 15) * 128 + ((c ^ (lane & 7)) << 4), src[0], src[1],
+                               src[2], src[3]);
+                }
+              }
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int row = 4 * j + (lane >> 3), c = lane & 7;
+                const uint4 v = ld_shared_v4(blk + row * 128 + ((c ^ (row & 7)) << 4));
+                *reinterpret_cast<uint4*>(
+                    obase + (((size_t)it.b * a.S + row0 + 16 * half + row) * a.H + h) * D + c * 8) = v;
+              }
+            }
+          }
+#pragma unroll 1
+          for (int hh = 0; hh < (D == 128 ? 2 : 0); ++hh) {
             uint32_t o[32], w[2][16];
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
