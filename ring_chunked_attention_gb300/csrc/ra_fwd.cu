@@ -388,12 +388,20 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 //   MMA_ORDER_GROUPED: both slots' PV products, then each slot's S after the
 //     commit of its PV.  The wait for slot 0 overlaps slot 1's PV, so the pipe
 //     does not drain, but the two slots' softmax warps run in phase and compete
-//     for the same issue slots: measured 17 % slower than the default on the
+//     for the same issue slots: measured 16 % slower than the default on the
 //     GQA workload.
 //   MMA_ORDER_INORDER: per slot, PV and the next S back to back with no wait,
 //     relying on the tensor pipe executing one thread's MMAs in issue order,
-//     which no document states; kept only to measure against (4.5 % faster
+//     which no document states; kept only to measure against (6 % faster
 //     than the default on the GQA workload).
+// A launch with one query tile per item (MODE_SINGLE) leaves slot 1 idle, so
+// the kernel is built a second time (SINGLE = true) with slot 0's P stored in
+// slot 1's S columns.  S_0(u+1) then rewrites nothing that PV_0(u) reads and
+// is issued without the wait, under every order.  The softmax writes P_0(u+1)
+// over P_0(u) only after the S_FULL commit of S_0(u+1), which arrives once
+// every earlier MMA of the thread, PV_0(u) included, has completed.  Measured
+// on the S = 4096 workload (256 single-tile items): 0.0642 against 0.0667 ms,
+// bit-identical; the paired kernels are unchanged.
 // The whole MMA warp runs the loop: every wait is taken by all 32 lanes
 // (a vote makes its outcome warp-uniform), and each tcgen05.mma and
 // tcgen05.commit is issued by the one lane elect.sync picks.  Measured against
@@ -434,12 +442,15 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, int ORDER>
+template <int D, int ORDER, bool P_APART>
 __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
                          volatile int* abort_flag) {
   using L = Layout<D>;
   auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
   const uint32_t tS0 = tmem + L::S_COL(0), tS1 = tmem + L::S_COL(1);
+  // one query tile per item: slot 0's P lives in slot 1's S columns, so the next
+  // S_0 does not rewrite it and needs no wait for the PV that reads it
+  const uint32_t tP0 = P_APART ? tS1 : tS0;
   const uint32_t tO0 = tmem + L::O_COL(0), tO1 = tmem + L::O_COL(1);
   const uint32_t q_lo0 = desc_lo(sbase + L::Q_OFF, 16);
   const uint32_t q_lo1 = desc_lo(sbase + L::Q_OFF + L::TILE, 16);
@@ -515,7 +526,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         if (n0) {
           if (!wait_all(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
-          issue_pv<D>(tO0, tS0, v_desc(st), !first0);
+          issue_pv<D>(tO0, tP0, v_desc(st), !first0);
           mma_commit_e(bar(L::O_FREE + 0));
           first0 = false;
         }
@@ -529,7 +540,8 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         mma_commit_e(bar(L::V_EMPTY + st));
         if (m0) {
           // the PV just issued for slot 0 (the O_FREE commit of S tile s_cnt0)
-          if (!wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          if (!P_APART &&
+              !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
           mma_commit_e(bar(L::S_FULL + 0));
@@ -549,12 +561,12 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         if (n0) {
           if (!wait_all(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
-          issue_pv<D>(tO0, tS0, v_desc(st), !first0);
+          issue_pv<D>(tO0, tP0, v_desc(st), !first0);
           mma_commit_e(bar(L::O_FREE + 0));
           first0 = false;
         }
         if (m0) {
-          if (ORDER == MMA_ORDER_STRICT &&
+          if (ORDER == MMA_ORDER_STRICT && !P_APART &&
               !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
@@ -730,8 +742,8 @@ __device__ __forceinline__ float row_max(const uint32_t (&va)[32], const uint32_
 // accepted): row max, new reference where the max passed m + threshold, O
 // rescale, exps again.
 template <int D, bool DIAG>
-__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, float c, bool first,
-                                             RowState& st, PackedRow& pk) {
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tP, uint32_t tO, int r, float c,
+                                             bool first, RowState& st, PackedRow& pk) {
   constexpr float kSpecLimit = 1073741824.0f;  // 2^30
   float se;
   {
@@ -782,15 +794,15 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int r, fl
     const uint64_t sum = f2_add(se0, se1);
     se = f2_lo(sum) + f2_hi(sum);
   }
-  tmem_st16(tS + 0, pk.a);
-  tmem_st16(tS + 16, pk.b);
-  tmem_st16(tS + 32, pk.c);
-  tmem_st16(tS + 48, pk.d);
+  tmem_st16(tP + 0, pk.a);
+  tmem_st16(tP + 16, pk.b);
+  tmem_st16(tP + 32, pk.c);
+  tmem_st16(tP + 48, pk.d);
   st.l_exact += se;
   tmem_wait_st();
 }
 
-template <int D>
+template <int D, bool SINGLE>
 __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
                              volatile int* abort_flag) {
   using L = Layout<D>;
@@ -800,6 +812,8 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   const int r = threadIdx.x & 127;  // row inside the 128-row query tile == TMEM lane
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
   const uint32_t tS = tmem + lane_base + L::S_COL(slot);
+  // one query tile per item: P goes to the unused slot's S columns, apart from S
+  const uint32_t tP = SINGLE ? tmem + lane_base + L::S_COL(1) : tS;
   const uint32_t tO = tmem + lane_base + L::O_COL(slot);
   const float c = a.scale_log2;
   uint32_t n = 0;  // S tiles consumed so far by this slot
@@ -840,9 +854,9 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       tc_fence_after();
       PackedRow pk;
       if (is_diag(a, my_qt, kt))
-        softmax_tile<D, true>(tS, tO, r, c, first, st, pk);
+        softmax_tile<D, true>(tS, tP, tO, r, c, first, st, pk);
       else
-        softmax_tile<D, false>(tS, tO, r, c, first, st, pk);
+        softmax_tile<D, false>(tS, tP, tO, r, c, first, st, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::P_FULL + slot));
@@ -962,7 +976,7 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   }
 }
 
-template <int D>
+template <int D, bool SINGLE>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -1008,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     regs_inc<kSoftmaxRegs>();
-    softmax_role<D>(a, sbase, tmem, abort_flag);
+    softmax_role<D, SINGLE>(a, sbase, tmem, abort_flag);
   } else {
     regs_dec<kProducerRegs>();
     if (warp == kWarpTma) {
@@ -1016,11 +1030,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma) {
       {
         if (a.mma_order == MMA_ORDER_GROUPED)
-          mma_role<D, MMA_ORDER_GROUPED>(a, sbase, tmem, abort_flag);
+          mma_role<D, MMA_ORDER_GROUPED, SINGLE>(a, sbase, tmem, abort_flag);
         else if (a.mma_order == MMA_ORDER_INORDER)
-          mma_role<D, MMA_ORDER_INORDER>(a, sbase, tmem, abort_flag);
+          mma_role<D, MMA_ORDER_INORDER, SINGLE>(a, sbase, tmem, abort_flag);
         else
-          mma_role<D, MMA_ORDER_STRICT>(a, sbase, tmem, abort_flag);
+          mma_role<D, MMA_ORDER_STRICT, SINGLE>(a, sbase, tmem, abort_flag);
       }
     }
   }
@@ -1049,21 +1063,25 @@ size_t fwd_smem_bytes(int D) {
   return D == 128 ? (size_t)Layout<128>::ALLOC : (size_t)Layout<64>::ALLOC;
 }
 
-template <int D>
+template <int D, bool SINGLE>
 static cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdArgs& args, int grid, cudaStream_t stream) {
   const int smem = Layout<D>::ALLOC;
   static std::atomic<unsigned> prepared[kMaxPrepDevices];
-  const cudaError_t e = prepare_kernel(ring_attn_fwd_kernel<D>, (int)kLaunchRegs, smem, prepared);
+  const cudaError_t e = prepare_kernel(ring_attn_fwd_kernel<D, SINGLE>, (int)kLaunchRegs, smem, prepared);
   if (e != cudaSuccess) return e;
-  ring_attn_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
+  ring_attn_fwd_kernel<D, SINGLE><<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& args, int grid, cudaStream_t stream) {
-  if (D == 128) return launch_d<128>(tq, tk, tv, args, grid, stream);
-  return launch_d<64>(tq, tk, tv, args, grid, stream);
+  const bool single = (args.mode == MODE_SINGLE);
+  if (D == 128)
+    return single ? launch_d<128, true>(tq, tk, tv, args, grid, stream)
+                  : launch_d<128, false>(tq, tk, tv, args, grid, stream);
+  return single ? launch_d<64, true>(tq, tk, tv, args, grid, stream)
+                : launch_d<64, false>(tq, tk, tv, args, grid, stream);
 }
 
 cudaError_t item_counter_ptr(unsigned int** p) {

@@ -387,22 +387,26 @@ def test_mma_orders_are_bit_identical(ralib, cuda_ok, name):
     accumulation order; they differ only in when the next S product of a query
     tile is issued relative to the PV product that reads the columns it
     rewrites.  Any ordering hazard would corrupt P and show up as a
-    difference.  Every workload, with paired query tiles forced (the pairs are
-    where the orders differ), and the default pairing for the default order."""
+    difference.  Every workload runs under every order twice: with paired query
+    tiles forced (the pairs are where the orders differ) and with one query
+    tile per item forced (P then sits in the idle slot's columns and the next S
+    is issued without waiting for the PV).  Pairing changes which SM runs a
+    tile, not its arithmetic, so all eight results are the same bits."""
     w = WORKLOADS[name] if name in WORKLOADS else Workload("small", 2, 8, 2, 2048, 128, 4, True)
     q, k, v = make_inputs(w, seed=43)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     outs = []
-    ralib.ra_set_item_pairing(1)
     try:
-        for order in (ralib.MMA_ORDER_STRICT, ralib.MMA_ORDER_GROUPED, ralib.MMA_ORDER_INORDER,
-                      ralib.MMA_ORDER_STRICT):
-            ralib.ra_set_mma_order(order)
-            o, l = ralib.ra_fwd(qd, kd, vd, P=w.P, causal=w.causal)
-            torch.cuda.synchronize()
-            assert ralib.ra_get_last_device_status() == 0
-            outs.append((o, l))
-            del o, l
+        for pairing in (1, 2):
+            ralib.ra_set_item_pairing(pairing)
+            for order in (ralib.MMA_ORDER_STRICT, ralib.MMA_ORDER_GROUPED,
+                          ralib.MMA_ORDER_INORDER, ralib.MMA_ORDER_STRICT):
+                ralib.ra_set_mma_order(order)
+                o, l = ralib.ra_fwd(qd, kd, vd, P=w.P, causal=w.causal)
+                torch.cuda.synchronize()
+                assert ralib.ra_get_last_device_status() == 0
+                outs.append((o, l))
+                del o, l
     finally:
         ralib.ra_set_mma_order(ralib.MMA_ORDER_STRICT)
         ralib.ra_set_item_pairing(0)
