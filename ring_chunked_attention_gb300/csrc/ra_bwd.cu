@@ -103,7 +103,10 @@ __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile in
 }
 
 // Bounded wait taken by all 32 lanes of a warp; the vote makes the outcome
-// warp-uniform (the MMA warps run their whole loop this way).
+// warp-uniform.  Every warp waits this way: one lane polling while the others
+// park at a __syncwarp cost the elementwise warps a divergent branch and a
+// reconvergence per tile (GQA backward 10.0 against 9.4 ms, D = 64 58.3
+// against 52.0 ms, bit-identical).
 __device__ __forceinline__ bool bwait_all(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           const BwdArgs& a) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
@@ -111,19 +114,11 @@ __device__ __forceinline__ bool bwait_all(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ bool bwait_warp(uint32_t bar, uint32_t parity,
-                                           volatile int* abort_flag, const BwdArgs& a) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = bwait(bar, parity, abort_flag, a) ? 1 : 0;
-  __syncwarp();
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// every elementwise warp arrives once
+// every elementwise warp arrives once (from the lane elect.sync picks)
 __device__ __forceinline__ void warp_arrive(uint32_t bar) {
   tc_fence_before();
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  mbar_arrive_e(bar);
 }
 
 // k-th work item of this CTA: snake order over rounds of gridDim.x items
@@ -486,8 +481,8 @@ __device__ void dkdv_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
       const bool diag = a.causal && cur.j == it.t;
       // the per-column arrays arrived by bulk copy with the step's dout tile:
       // acquire them through that stage's barrier
-      if (!bwait_warp(bar(L::DO_FULL + g % L::ND), (g / L::ND) & 1, abort_flag, a)) return;
-      if (!bwait_warp(bar(L::S_FULL), g & 1, abort_flag, a)) return;
+      if (!bwait_all(bar(L::DO_FULL + g % L::ND), (g / L::ND) & 1, abort_flag, a)) return;
+      if (!bwait_all(bar(L::S_FULL), g & 1, abort_flag, a)) return;
       tc_fence_after();
       uint32_t sa[32], sb[32];
       tmem_ld32(tS + 0, sa);
@@ -505,7 +500,7 @@ __device__ void dkdv_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
       }
       // dS^T = P^T (dP^T - delta).  This half's 64 dP^T columns, once read,
       // take P^T (first 32) and dS^T (last 32) as bf16 pairs.
-      if (!bwait_warp(bar(L::DP_FULL), g & 1, abort_flag, a)) return;
+      if (!bwait_all(bar(L::DP_FULL), g & 1, abort_flag, a)) return;
       tc_fence_after();
       uint32_t va[32], vb[32], pk[16];
       tmem_ld32(tDP + 0, va);
@@ -524,7 +519,7 @@ __device__ void dkdv_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
       warp_arrive(bar(L::PDS_FULL));
     }
     // epilogue: this warpgroup's half of the dv and dk rows of this key
-    if (!bwait_warp(bar(L::ACC_DONE), n_done & 1, abort_flag, a)) return;
+    if (!bwait_all(bar(L::ACC_DONE), n_done & 1, abort_flag, a)) return;
     ++n_done;
     tc_fence_after();
     const size_t row = ((size_t)it.b * a.S + (size_t)it.t * kT + r) * a.Hkv + it.kvh;
@@ -748,7 +743,7 @@ __device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
     cur.init(a, it.j);
     for (int u = 0; u < ns; ++u, ++g, cur.next()) {
       const bool diag = a.causal && cur.kt == it.j;
-      if (!bwait_warp(bar(L::S_FULL), g & 1, abort_flag, a)) return;
+      if (!bwait_all(bar(L::S_FULL), g & 1, abort_flag, a)) return;
       tc_fence_after();
       uint32_t sa[32], sb[32];
       tmem_ld32(tS + 0, sa);
@@ -764,9 +759,9 @@ __device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
         exp_chunk<false, false>(sa, c0, r, c2, nl2x2, nullptr);
         exp_chunk<false, false>(sb, c0 + 32, r, c2, nl2x2, nullptr);
       }
-      if (!bwait_warp(bar(L::DP_FULL), g & 1, abort_flag, a)) return;
+      if (!bwait_all(bar(L::DP_FULL), g & 1, abort_flag, a)) return;
       // the previous step's dq MMA has read the dS columns
-      if (g > 0 && !bwait_warp(bar(L::DQ_DONE), (g - 1) & 1, abort_flag, a)) return;
+      if (g > 0 && !bwait_all(bar(L::DQ_DONE), (g - 1) & 1, abort_flag, a)) return;
       tc_fence_after();
       uint32_t va[32], vb[32], pk[16];
       tmem_ld32(tDP + 0, va);
@@ -782,7 +777,7 @@ __device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
       warp_arrive(bar(L::DS_FULL));
     }
     // epilogue: this warpgroup's half of the dq row = scale * accumulator
-    if (!bwait_warp(bar(L::DQ_DONE), (g - 1) & 1, abort_flag, a)) return;
+    if (!bwait_all(bar(L::DQ_DONE), (g - 1) & 1, abort_flag, a)) return;
     tc_fence_after();
     const size_t row = ((size_t)it.b * a.S + (size_t)it.j * kT + r) * a.H + it.h;
     const int e0 = (warp >> 2) * (DH / 2);

@@ -203,6 +203,16 @@ __device__ __forceinline__ void mma_ts_lh_e(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// one arrive on an mbarrier for the whole warp, from the lane elect.sync picks
+// (a predicated instruction: no divergent branch)
+__device__ __forceinline__ void mbar_arrive_e(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_e(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
