@@ -725,8 +725,9 @@ def main():
                          "instead of running one replica per rank")
     ap.add_argument("--virtual-ranks", type=int, default=0,
                     help="with --ring on one GPU: emulate this many ranks in one process")
-    ap.add_argument("--mma-order", type=int, default=0, choices=[0, 1, 2],
-                    help="forward MMA issue order (0 strict, the default; 1 grouped; 2 in-order)")
+    ap.add_argument("--mma-order", type=int, default=3, choices=[0, 1, 2, 3],
+                    help="forward MMA issue order (3 bridged by a tcgen05.shift, the default; "
+                         "0 strict commit wait; 1 grouped; 2 in-order)")
     ap.add_argument("--full-oracle", action="store_true",
                     help="time the CPU oracle on every row of the workload instead of a sample "
                          "(minutes at the long-context sizes)")

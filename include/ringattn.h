@@ -267,19 +267,24 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
  * tile are kept in tensor memory over the columns of the score tile S_i that
  * produced them, so the next S_i = Q_i K^T must not start before
  * O_i += P_i V has read them.  The PTX ISA orders two tcgen05.mma of one
- * thread only when they share the accumulator; it orders completion as seen
- * through tcgen05.commit and an mbarrier wait.
- *   order 0 (default): per key/value step and query tile in turn, PV, a wait
- *     for its commit, the next S.  Every rewrite of P's columns is ordered by
- *     commit and wait; the tensor pipe drains once per tile.
+ * thread directly only when they share the accumulator.  It also lists
+ * tcgen05.mma -> tcgen05.shift and tcgen05.shift -> tcgen05.mma (same
+ * cta_group) among the pairs that execute in issue order, and it orders
+ * completion as seen through tcgen05.commit and an mbarrier wait.
+ *   order 3 (default): per key/value step and query tile in turn, PV, a
+ *     tcgen05.shift of 8 columns of S_i that hold consumed scores, the next
+ *     S.  PV -> shift -> S execute in issue order, with no wait.
+ *   order 0: the same with a wait for the PV's commit instead of the shift.
+ *     Ordered by completion; the tensor pipe drains once per tile.
  *   order 1: per key/value step, both query tiles' PV products, then each
  *     tile's next S once the commit of its PV has arrived (no drain, but the
  *     two tiles' softmax work runs at the same time and competes; slower).
- *   order 2: per tile in turn, PV and the next S back to back with no wait,
- *     relying on the tensor pipe executing one thread's MMAs in issue order,
- *     which no document states.  For measurement and tests only.
- * All three compute the same arithmetic; the test-suite checks that their
- * outputs are bit-identical.  Other values select order 0.  Applies to
+ *   order 2: per tile in turn, PV and the next S back to back with nothing
+ *     between, relying on the tensor pipe executing MMAs with different
+ *     accumulators in issue order, which no document states.  For measurement
+ *     and tests only.
+ * All four compute the same arithmetic; the test-suite checks that their
+ * outputs are bit-identical.  Other values select order 3.  Applies to
  * launches made after the call.
  */
 void ra_set_mma_order(int order);

@@ -23,6 +23,7 @@ import os
 __all__ = ["ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_measure_ceilings", "ra_get_last_device_status", "ra_status_string",
            "ra_debug_set_fault", "ra_set_mma_order", "ra_set_item_pairing", "ra_shutdown", "ra_version",
            "RaError", "library_path", "MMA_ORDER_GROUPED", "MMA_ORDER_STRICT", "MMA_ORDER_INORDER",
+           "MMA_ORDER_BRIDGED",
            "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT"]
 
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = 0, 1, 2, 3, 4
@@ -339,13 +340,14 @@ def ra_debug_set_fault(timeout_ns: int, skip_value_load: bool) -> None:
     _load().ra_debug_set_fault(int(timeout_ns), int(bool(skip_value_load)))
 
 
-MMA_ORDER_STRICT, MMA_ORDER_GROUPED, MMA_ORDER_INORDER = 0, 1, 2
+MMA_ORDER_STRICT, MMA_ORDER_GROUPED, MMA_ORDER_INORDER, MMA_ORDER_BRIDGED = 0, 1, 2, 3
 
 
 def ra_set_mma_order(order: int) -> None:
     """MMA issue order of subsequent ra_fwd / ra_fwd_block launches:
-    0 strict (default), 1 grouped, 2 in-order without waits (for measurement
-    only); see include/ringattn.h."""
+    3 bridged by a tcgen05.shift (default), 0 strict (commit wait), 1 grouped,
+    2 in-order with nothing between (for measurement only); see
+    include/ringattn.h."""
     _load().ra_set_mma_order(int(order))
 
 

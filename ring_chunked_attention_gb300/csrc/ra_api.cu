@@ -32,7 +32,7 @@ std::atomic<unsigned> g_prep_epoch{0};
 namespace {
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 int g_skip_value_load = 0;
-int g_mma_order = 0;  // ra::MmaOrder
+int g_mma_order = ra::MMA_ORDER_BRIDGED;  // ra::MmaOrder
 int g_item_pairing = 0;  // 0 automatic, 1 always pair when the shape allows, 2 never pair
 
 // per-device facts, queried once
@@ -484,9 +484,10 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load) {
 
 void ra_set_mma_order(int order) {
   std::lock_guard<std::mutex> lock(g_mu);
-  g_mma_order = (order == ra::MMA_ORDER_GROUPED || order == ra::MMA_ORDER_INORDER)
+  g_mma_order = (order == ra::MMA_ORDER_STRICT || order == ra::MMA_ORDER_GROUPED ||
+                 order == ra::MMA_ORDER_INORDER)
                     ? order
-                    : ra::MMA_ORDER_STRICT;
+                    : ra::MMA_ORDER_BRIDGED;
 }
 
 void ra_set_item_pairing(int policy) {
@@ -501,7 +502,7 @@ void ra_shutdown(void) {
   for (auto& d : g_dev) d = DeviceInfo{};
   g_timeout_ns = kDefaultTimeoutNs;
   g_skip_value_load = 0;
-  g_mma_order = 0;
+  g_mma_order = ra::MMA_ORDER_BRIDGED;
   g_item_pairing = 0;
 }
 

@@ -382,25 +382,33 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 // ---------------------------------------------------------------- MMA issuer
 // P_i(u) is written over the first columns of S_i, so S_i(u+1) = Q_i K(u+1)^T
 // must not start before O_i += P_i(u) V(u) has read them.  The PTX ISA orders
-// two tcgen05.mma of one thread only when they share the accumulator (and
-// shape); these two do not.  What it does order is completion as observed
-// through tcgen05.commit: the commit's mbarrier arrive happens once every
-// tcgen05 operation the thread issued before it has completed.  The issue
-// orders:
-//   MMA_ORDER_STRICT (default): per key/value step u, for each slot in turn:
-//     O_i += P_i(u) V(u), committed to the slot's O_FREE barrier; a wait for
-//     that commit; S_i(u+1) = Q_i K(u+1)^T.  Every rewrite of P's columns is
-//     ordered by commit and wait; the tensor pipe drains once per tile (the
-//     last PV MMA's execution plus the commit's round trip).
+// two tcgen05.mma of one thread directly only when they share the accumulator
+// (and shape); these two do not.  It lists other pairs of tcgen05 operations
+// that execute in issue order, among them tcgen05.mma -> tcgen05.shift and
+// tcgen05.shift -> tcgen05.mma (same cta_group), and it orders completion as
+// observed through tcgen05.commit and an mbarrier wait.  The issue orders:
+//   MMA_ORDER_BRIDGED (default): per key/value step u, for each slot in turn:
+//     O_i += P_i(u) V(u); a tcgen05.shift of one 32-byte column block of S_i
+//     that holds consumed scores (columns 64-71: not P, and rewritten by the
+//     next S anyway); S_i(u+1).  PV -> shift -> S execute in issue order by
+//     the two pairs above, so S_i(u+1) writes its columns after the PV has
+//     read P, with no wait and no drain of the pipe.  GQA workload 2.80
+//     against 3.15 ms for the commit-wait form, D = 64 18.1 against 18.5 ms,
+//     bit-identical.
+//   MMA_ORDER_STRICT: the same, with a wait for the PV's commit (O_FREE)
+//     instead of the shift: ordered by completion; the tensor pipe drains once
+//     per tile (the last PV MMA's execution plus the commit's round trip).
 //   MMA_ORDER_GROUPED: both slots' PV products, then each slot's S after the
 //     commit of its PV.  The wait for slot 0 overlaps slot 1's PV, so the pipe
 //     does not drain, but the two slots' softmax warps run in phase and compete
-//     for the same issue slots: measured 16 % slower than the default on the
-//     GQA workload.
-//   MMA_ORDER_INORDER: per slot, PV and the next S back to back with no wait,
-//     relying on the tensor pipe executing one thread's MMAs in issue order,
-//     which no document states; kept only to measure against (6 % faster
-//     than the default on the GQA workload).
+//     for the same exp and issue slots: 3.21 against 3.15 ms (strict).
+//   MMA_ORDER_INORDER: per slot, PV and the next S back to back with nothing
+//     between, relying on the tensor pipe executing two MMAs with different
+//     accumulators in issue order, which no document states; kept only to
+//     measure against (2.72 ms on the GQA workload).
+// The first S of an item still waits for the commit of the slot's last PV of
+// the previous item (bridging it as well was slower: 18.6 against 18.1 ms at
+// D = 64).
 // A launch with one query tile per item (MODE_SINGLE) leaves slot 1 idle, so
 // the kernel is built a second time (SINGLE = true) with slot 0's P stored in
 // slot 1's S columns.  S_0(u+1) then rewrites nothing that PV_0(u) reads and
@@ -564,6 +572,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           first0 = false;
         }
         if (m0) {
+          if (ORDER == MMA_ORDER_BRIDGED && !P_APART) tmem_shift_down_e(tS0 + 64u);
           if (ORDER == MMA_ORDER_STRICT && !P_APART &&
               !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
@@ -580,6 +589,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           first1 = false;
         }
         if (m1) {
+          if (ORDER == MMA_ORDER_BRIDGED) tmem_shift_down_e(tS1 + 64u);
           if (ORDER == MMA_ORDER_STRICT && s_cnt1 > 0 &&
               !wait_all(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
@@ -1031,6 +1041,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_role<D, MMA_ORDER_GROUPED, SINGLE>(a, sbase, tmem, abort_flag);
         else if (a.mma_order == MMA_ORDER_INORDER)
           mma_role<D, MMA_ORDER_INORDER, SINGLE>(a, sbase, tmem, abort_flag);
+        else if (a.mma_order == MMA_ORDER_BRIDGED)
+          mma_role<D, MMA_ORDER_BRIDGED, SINGLE>(a, sbase, tmem, abort_flag);
         else
           mma_role<D, MMA_ORDER_STRICT, SINGLE>(a, sbase, tmem, abort_flag);
       }

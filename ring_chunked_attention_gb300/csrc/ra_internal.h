@@ -18,9 +18,10 @@ enum PairMode : int {
 
 // Issue order of the forward's MMA thread (see ra_fwd.cu, "MMA issuer").
 enum MmaOrder : int {
-  MMA_ORDER_STRICT = 0,   // per slot: PV, wait for its commit, next S (default)
+  MMA_ORDER_STRICT = 0,   // per slot: PV, wait for its commit, next S
   MMA_ORDER_GROUPED = 1,  // both slots' PV, then each next S after its PV's commit
   MMA_ORDER_INORDER = 2,  // per slot: PV and next S back to back (relies on in-order execution)
+  MMA_ORDER_BRIDGED = 3,  // per slot: PV, a tcgen05.shift of dead S columns, next S (default)
 };
 
 // Kernel arguments besides the three tensor maps (q, k, v).

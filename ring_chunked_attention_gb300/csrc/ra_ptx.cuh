@@ -213,6 +213,16 @@ __device__ __forceinline__ void mbar_arrive_e(uint32_t bar) {
       : "memory");
 }
 
+// tcgen05.shift.down of the 32-byte column block at taddr (lane 0), issued by
+// the lane elect.sync picks
+__device__ __forceinline__ void tmem_shift_down_e(uint32_t taddr) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.shift.cta_group::1.down [%0];\n\t}" ::"r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_e(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"

@@ -383,15 +383,16 @@ def test_stream_argument_is_used(ralib, cuda_ok, oracle_mod):
 @pytest.mark.parametrize("name", ["tiny", "causal_s4096", "gqa_s16384", "long_s65536",
                                   "d64_s32768", "small"])
 def test_mma_orders_are_bit_identical(ralib, cuda_ok, name):
-    """The three MMA issue orders run the same arithmetic in the same
-    accumulation order; they differ only in when the next S product of a query
-    tile is issued relative to the PV product that reads the columns it
-    rewrites.  Any ordering hazard would corrupt P and show up as a
-    difference.  Every workload runs under every order twice: with paired query
-    tiles forced (the pairs are where the orders differ) and with one query
-    tile per item forced (P then sits in the idle slot's columns and the next S
-    is issued without waiting for the PV).  Pairing changes which SM runs a
-    tile, not its arithmetic, so all eight results are the same bits."""
+    """The four MMA issue orders run the same arithmetic in the same
+    accumulation order; they differ only in how the next S product of a query
+    tile is ordered after the PV product that reads the columns it rewrites
+    (a tcgen05.shift between them, a commit wait, both PVs first, or nothing).
+    Any ordering hazard would corrupt P and show up as a difference.  Every
+    workload runs under every order twice: with paired query tiles forced (the
+    pairs are where the orders differ) and with one query tile per item forced
+    (P then sits in the idle slot's columns and the next S is issued without
+    waiting for the PV).  Pairing changes which SM runs a tile, not its
+    arithmetic, so all ten results are the same bits."""
     w = WORKLOADS[name] if name in WORKLOADS else Workload("small", 2, 8, 2, 2048, 128, 4, True)
     q, k, v = make_inputs(w, seed=43)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
@@ -399,8 +400,9 @@ def test_mma_orders_are_bit_identical(ralib, cuda_ok, name):
     try:
         for pairing in (1, 2):
             ralib.ra_set_item_pairing(pairing)
-            for order in (ralib.MMA_ORDER_STRICT, ralib.MMA_ORDER_GROUPED,
-                          ralib.MMA_ORDER_INORDER, ralib.MMA_ORDER_STRICT):
+            for order in (ralib.MMA_ORDER_BRIDGED, ralib.MMA_ORDER_STRICT,
+                          ralib.MMA_ORDER_GROUPED, ralib.MMA_ORDER_INORDER,
+                          ralib.MMA_ORDER_BRIDGED):
                 ralib.ra_set_mma_order(order)
                 o, l = ralib.ra_fwd(qd, kd, vd, P=w.P, causal=w.causal)
                 torch.cuda.synchronize()
@@ -408,7 +410,7 @@ def test_mma_orders_are_bit_identical(ralib, cuda_ok, name):
                 outs.append((o, l))
                 del o, l
     finally:
-        ralib.ra_set_mma_order(ralib.MMA_ORDER_STRICT)
+        ralib.ra_set_mma_order(ralib.MMA_ORDER_BRIDGED)
         ralib.ra_set_item_pairing(0)
     for o, l in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
