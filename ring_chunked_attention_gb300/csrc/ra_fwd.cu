@@ -525,8 +525,18 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       const bool m0 = more && nxt.kt <= lim0, m1 = more && nxt.kt <= lim1;
       const int st1 = (c + 1) % L::NS;
       if (!wait_all(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
-      if (more &&
-          !wait_all(bar(L::K_FULL + st1), ((c + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+      // K(u+1) is needed only by the next S products.  At D = 128 (a 2-deep
+      // ring) it is waited for after slot 0's PV, which gives its copy that much
+      // longer to land: GQA 2.72 against 2.81 ms.  At D = 64 the 5-deep ring has
+      // it in place, and the later wait only lengthens the chain (18.6 against
+      // 18.1 ms), so it stays at the top of the step there.
+      constexpr bool kLateK = (D == 128 && ORDER == MMA_ORDER_BRIDGED);
+      bool k_ready = !more;
+      if (!kLateK) {
+        if (more &&
+            !wait_all(bar(L::K_FULL + st1), ((c + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+        k_ready = true;
+      }
       if (ORDER == MMA_ORDER_GROUPED) {
         // both PV products, then each slot's next S once its PV has completed
         if (n0) {
@@ -570,6 +580,10 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           issue_pv<D>(tO0, tP0, v_desc(st), !first0);
           mma_commit_e(bar(L::O_FREE + 0));
           first0 = false;
+        }
+        if (more && !k_ready) {
+          if (!wait_all(bar(L::K_FULL + st1), ((c + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+          k_ready = true;
         }
         if (m0) {
           if (ORDER == MMA_ORDER_BRIDGED && !P_APART) tmem_shift_down_e(tS0 + 64u);
