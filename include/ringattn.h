@@ -56,8 +56,11 @@ typedef enum ra_status {
                              B*H*S/128) */
   RA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute query,
                              tensor-map encode); ra_last_cuda_error() gives the code */
-  RA_ERR_TIMEOUT = 4      /* a bounded wait inside a kernel gave up (reported by
+  RA_ERR_TIMEOUT = 4,     /* a bounded wait inside a kernel gave up (reported by
                              ra_get_last_device_status) */
+  RA_ERR_BOUNDS = 5       /* bounds-checked builds only (ra_debug_build() == 1): a kernel
+                             computed a global address outside its buffer and skipped the
+                             access (reported by ra_get_last_device_status) */
 } ra_status;
 
 /*
@@ -216,8 +219,10 @@ ra_status ra_bwd_static(const void* q, const void* k, const void* v, const void*
  * valid), RA_ERR_UNSUPPORTED if a kernel refused to run because the runtime
  * gave it a shared-memory base that is not 1024-byte aligned (the dk/dv kernel
  * of ra_bwd needs nearly all of a CTA's shared memory and cannot round the base
- * up; its outputs are then not written), RA_ERR_CUDA if the synchronisation
- * itself failed, else RA_OK.
+ * up; its outputs are then not written), RA_ERR_BOUNDS (bounds-checked builds
+ * only) if a kernel skipped an access outside a buffer, RA_ERR_CUDA if the
+ * synchronisation itself failed, else RA_OK.  With several bits set, the first
+ * of timeout, bounds, layout in that order is reported.
  */
 ra_status ra_get_last_device_status(void* stream);
 
@@ -260,6 +265,26 @@ int ra_version(void);
  * normal launches.
  */
 void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
+
+/*
+ * Bounds-checked builds (no counterpart on the pages; a test facility).  The
+ * library compiled with RA_DEBUG (libringattn_debug.so, built by
+ * `python -m ring_chunked_attention_gb300.build --debug`) checks every global
+ * address its kernels compute (output, lse, gradient and workspace rows, the
+ * merge's partials; the tensor-map copies are bounded by the hardware) against
+ * the buffer's size as the call's arguments give it.  An address outside it
+ * sets a status bit and the access is skipped, with no trap: the next
+ * ra_get_last_device_status returns RA_ERR_BOUNDS.  Other builds compile the
+ * checks away.
+ *   ra_debug_build: 1 in a bounds-checked build, 0 otherwise.
+ *   ra_debug_set_bounds_trim: a test hook for bounds-checked builds; the last
+ *     `elements` elements of every checked buffer count as outside it, so a
+ *     test can see the checks fire without any access outside a buffer.  0
+ *     (the default; negative values too) turns it off.  No effect in other
+ *     builds.  Applies to launches made after the call.
+ */
+int ra_debug_build(void);
+void ra_debug_set_bounds_trim(long long elements);
 
 /*
  * MMA issue order of ra_fwd and ra_fwd_block (no counterpart on the pages; an

@@ -24,17 +24,21 @@ __all__ = ["ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspac
            "ra_debug_set_fault", "ra_set_mma_order", "ra_set_item_pairing", "ra_shutdown", "ra_version",
            "RaError", "library_path", "MMA_ORDER_GROUPED", "MMA_ORDER_STRICT", "MMA_ORDER_INORDER",
            "MMA_ORDER_BRIDGED",
-           "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT"]
+           "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT",
+           "RA_ERR_BOUNDS", "ra_debug_build", "ra_debug_set_bounds_trim"]
 
-RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT, RA_ERR_BOUNDS = (
+    0, 1, 2, 3, 4, 5)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libringattn.so")
+# RA_DEBUG=1 selects the bounds-checked build (python -m ring_chunked_attention_gb300.build --debug)
+_DEBUG = os.environ.get("RA_DEBUG", "0") == "1"
+_LIB_PATH = os.path.join(_HERE, "libringattn_debug.so" if _DEBUG else "libringattn.so")
 _lib = None
 
 EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_measure_ceilings", "ra_get_last_device_status", "ra_status_string",
            "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_set_mma_order",
-           "ra_set_item_pairing", "ra_shutdown")
+           "ra_set_item_pairing", "ra_shutdown", "ra_debug_build", "ra_debug_set_bounds_trim")
 
 
 class RaError(RuntimeError):
@@ -53,8 +57,9 @@ def _load():
     if _lib is not None:
         return _lib
     if not os.path.exists(_LIB_PATH):
-        raise RuntimeError(f"libringattn.so is not built ({_LIB_PATH}); run "
-                           "`python -m ring_chunked_attention_gb300.build`")
+        raise RuntimeError(f"{os.path.basename(_LIB_PATH)} is not built ({_LIB_PATH}); run "
+                           "`python -m ring_chunked_attention_gb300.build`"
+                           + (" --debug" if _DEBUG else ""))
     lib = ctypes.CDLL(_LIB_PATH)
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.ra_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
@@ -89,6 +94,10 @@ def _load():
     lib.ra_set_item_pairing.restype = None
     lib.ra_shutdown.argtypes = []
     lib.ra_shutdown.restype = None
+    lib.ra_debug_build.argtypes = []
+    lib.ra_debug_build.restype = i
+    lib.ra_debug_set_bounds_trim.argtypes = [ctypes.c_longlong]
+    lib.ra_debug_set_bounds_trim.restype = None
     _lib = lib
     return lib
 
@@ -349,6 +358,17 @@ def ra_set_mma_order(order: int) -> None:
     2 in-order with nothing between (for measurement only); see
     include/ringattn.h."""
     _load().ra_set_mma_order(int(order))
+
+
+def ra_debug_build() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(_load().ra_debug_build())
+
+
+def ra_debug_set_bounds_trim(elements: int) -> None:
+    """Bounds-checked builds: the last ``elements`` elements of every checked
+    buffer count as outside it (a test hook; 0 turns it off)."""
+    _load().ra_debug_set_bounds_trim(int(elements))
 
 
 def ra_set_item_pairing(policy: int) -> None:

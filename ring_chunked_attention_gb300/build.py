@@ -2,7 +2,11 @@
 
 Each ``csrc/*.cu`` compiles to an object in parallel, then one link step.
 The result lands beside this file (git-ignored).  Run as a script or call
-:func:`build`.
+:func:`build`.  ``--debug`` (``build(debug=True)``) builds the bounds-checked
+flavour instead, ``libringattn_debug.so`` (compiled with ``RA_DEBUG``: every
+global address a kernel computes is checked against its buffer; see
+``include/ringattn.h``), which the binding loads when the environment variable
+``RA_DEBUG`` is ``1``.
 """
 from __future__ import annotations
 
@@ -18,6 +22,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libringattn.so")
+DEBUG_LIB = os.path.join(HERE, "libringattn_debug.so")
 SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_merge.cu", "ra_ceil.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -34,24 +39,27 @@ def _flags(extra=()):
                    "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr", *extra]
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "ringattn.h"),
                                                                os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    lib = DEBUG_LIB if debug else LIB
+    if not force and not _stale(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    build_dir = BUILD_DIR + ("_debug" if debug else "")
+    os.makedirs(build_dir, exist_ok=True)
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DRA_DEBUG"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nvcc, *_flags(extra), "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,14 +72,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, err in results:
             if err:
                 sys.stderr.write(err)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="-v" in sys.argv,
+                debug="--debug" in sys.argv))

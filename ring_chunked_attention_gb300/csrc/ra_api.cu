@@ -34,6 +34,7 @@ unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 int g_skip_value_load = 0;
 int g_mma_order = ra::MMA_ORDER_BRIDGED;  // ra::MmaOrder
 int g_item_pairing = 0;  // 0 automatic, 1 always pair when the shape allows, 2 never pair
+long long g_bounds_trim = 0;  // bounds-checked builds: test hook (ra_debug_set_bounds_trim)
 
 // per-device facts, queried once
 struct DeviceInfo {
@@ -234,6 +235,7 @@ ra_status launch_attention(const void* q, const void* k, const void* v, void* ou
     a.timeout_ns = g_timeout_ns;
     a.skip_value_load = g_skip_value_load;
     a.mma_order = g_mma_order;
+    a.bounds_trim = g_bounds_trim;
     pairing = g_item_pairing;
     // each eager launch takes the next of the eager slots (the kernel leaves
     // it at zero); a captured launch takes a captured slot that no other
@@ -319,8 +321,13 @@ ra_status ra_merge_partials(const void* o_parts, int o_is_fp32, const float* lse
   if (!dev->sm103) return RA_ERR_UNSUPPORTED;
   const long long rows = (long long)B * S * H;
   if (rows >= (1ll << 31)) return RA_ERR_UNSUPPORTED;
+  long long trim;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    trim = g_bounds_trim;
+  }
   cudaError_t e = ra::launch_merge(o_parts, o_is_fp32, lse_parts, n, out, lse, B, H, S, D,
-                                   dev->sms, static_cast<cudaStream_t>(stream));
+                                   dev->sms, dev->status, trim, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return RA_OK;
 }
@@ -392,6 +399,7 @@ ra_status launch_backward(DeviceInfo* dev, const void* q, const void* k, const v
     std::lock_guard<std::mutex> lock(g_mu);
     a.timeout_ns = g_timeout_ns;
     a.skip_first_load = g_skip_value_load;
+    a.bounds_trim = g_bounds_trim;
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long units = (long long)B * S * H * (D / 8);
@@ -458,6 +466,7 @@ ra_status ra_get_last_device_status(void* stream) {
   e = ra::read_and_clear_status(&v);
   if (e != cudaSuccess) return cuda_fail(e);
   if (v & ra::kStatusTimeout) return RA_ERR_TIMEOUT;
+  if (v & ra::kStatusBounds) return RA_ERR_BOUNDS;
   return (v & ra::kStatusLayout) ? RA_ERR_UNSUPPORTED : RA_OK;
 }
 
@@ -468,6 +477,7 @@ const char* ra_status_string(ra_status s) {
     case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED";
     case RA_ERR_CUDA: return "RA_ERR_CUDA";
     case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT";
+    case RA_ERR_BOUNDS: return "RA_ERR_BOUNDS";
   }
   return "RA_ERR_UNKNOWN";
 }
@@ -480,6 +490,19 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_timeout_ns = timeout_ns > 0 ? (unsigned long long)timeout_ns : kDefaultTimeoutNs;
   g_skip_value_load = skip_value_load ? 1 : 0;
+}
+
+void ra_debug_set_bounds_trim(long long elements) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_bounds_trim = elements > 0 ? elements : 0;
+}
+
+int ra_debug_build(void) {
+#ifdef RA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 void ra_set_mma_order(int order) {
@@ -504,6 +527,7 @@ void ra_shutdown(void) {
   g_skip_value_load = 0;
   g_mma_order = ra::MMA_ORDER_BRIDGED;
   g_item_pairing = 0;
+  g_bounds_trim = 0;
 }
 
 }  // extern "C"

@@ -178,9 +178,10 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&p)[32], const uint32_t
 }
 
 // NC fp32 accumulator columns of this thread's TMEM lane -> bf16 in global
-// memory at dst, times `mul`.
+// memory at dst, times `mul` (the loads run whatever `ok` says: they are
+// warp-collective; the stores only when it is true).
 template <int NC>
-__device__ __forceinline__ void store_row(uint32_t tAcc, float mul, __nv_bfloat16* dst) {
+__device__ __forceinline__ void store_row(uint32_t tAcc, float mul, __nv_bfloat16* dst, bool ok) {
   uint4* row = reinterpret_cast<uint4*>(dst);
 #pragma unroll 1
   for (int c0 = 0; c0 < NC; c0 += 32) {
@@ -192,7 +193,7 @@ __device__ __forceinline__ void store_row(uint32_t tAcc, float mul, __nv_bfloat1
     for (int j = 0; j < 16; ++j)
       w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < 4 && ok; ++j)
       row[c0 / 8 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
   }
 }
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
   constexpr int per = DH / 8;
   const long long rows = (long long)a.B * a.S * a.H;  // [B,S,H] order
   const long long units = rows * per;
+  const long long elems = rows * DH;  // elements of out and dout
   const int lane = threadIdx.x & 31;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long w0 = (long long)blockIdx.x * blockDim.x + (threadIdx.x - lane); w0 < units;
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
     const long long row = w / per;
     const int cpart = (int)(w - row * per);
     float acc = 0.0f;
-    if (active) {
+    if (active && in_bounds(row * DH + cpart * 8, 8, elems, a.bounds_trim, a.status)) {
       const long long e0 = row * DH + cpart * 8;
       const uint4 o = __ldcs(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out) + e0));
       const uint4 g = __ldcs(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + e0));
@@ -233,8 +235,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdArgs a) {
       const int s = (int)(bs % a.S);
       const long long b = bs / a.S;
       const long long li = (b * a.H + h) * a.S + s;
-      a.ndelta[li] = -acc;
-      a.nlse2[li] = -a.lse[li] * kLog2e;
+      if (in_bounds(li, 1, rows, a.bounds_trim, a.status)) {
+        a.ndelta[li] = -acc;
+        a.nlse2[li] = -a.lse[li] * kLog2e;
+      }
     }
   }
 }
@@ -354,7 +358,10 @@ __device__ void dkdv_tma(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
       if (!(a.skip_first_load && g == 0))  // test hook: the stage then never completes
         for (int kb = 0; kb < L::DK; ++kb)
           tma_load_3d(stage + kb * kBlk, tdo, fb, kb * 64, h, qrow, pol_keep);
-      const size_t li = ((size_t)it.b * a.H + h) * a.S + (size_t)cur.j * kT;
+      size_t li = ((size_t)it.b * a.H + h) * a.S + (size_t)cur.j * kT;
+      // outside the workspace (bounds-checked builds): copy from its start, so
+      // that the stage's barrier still completes
+      if (!in_bounds(li, kT, (size_t)a.B * a.H * a.S, a.bounds_trim, a.status)) li = 0;
       bulk_load(stage + L::NL2_IN, a.nlse2 + li, 512, fb);
       bulk_load(stage + L::DL_IN, a.ndelta + li, 512, fb);
     }
@@ -528,8 +535,10 @@ __device__ void dkdv_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
     tc_fence_after();
     const size_t row = ((size_t)it.b * a.S + (size_t)it.t * kT + r) * a.Hkv + it.kvh;
     const int e0 = (warp >> 2) * (DH / 2);
-    store_row<DH / 2>(tDV + e0, 1.0f, static_cast<__nv_bfloat16*>(a.dv) + row * DH + e0);
-    store_row<DH / 2>(tDK + e0, a.scale, static_cast<__nv_bfloat16*>(a.dk) + row * DH + e0);
+    const bool ok = in_bounds(row * DH + e0, DH / 2, (size_t)a.B * a.S * a.Hkv * DH, a.bounds_trim,
+                              a.status);
+    store_row<DH / 2>(tDV + e0, 1.0f, static_cast<__nv_bfloat16*>(a.dv) + row * DH + e0, ok);
+    store_row<DH / 2>(tDK + e0, a.scale, static_cast<__nv_bfloat16*>(a.dk) + row * DH + e0, ok);
     tc_fence_before();
   }
 }
@@ -741,7 +750,8 @@ __device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
     const DqItem it = dq_item(a, x);
     const int ns = a.causal ? it.j + 1 : a.tiles;
     const size_t li = ((size_t)it.b * a.H + it.h) * a.S + (size_t)it.j * kT + r;
-    const float nl2 = a.nlse2[li], ndl = a.ndelta[li];
+    const bool li_ok = in_bounds(li, 1, (size_t)a.B * a.H * a.S, a.bounds_trim, a.status);
+    const float nl2 = li_ok ? a.nlse2[li] : 0.0f, ndl = li_ok ? a.ndelta[li] : 0.0f;
     const uint64_t nl2x2 = f2_pack(nl2, nl2), ndl2 = f2_pack(ndl, ndl);
     RingCursor cur;
     cur.init(a, it.j);
@@ -785,7 +795,9 @@ __device__ void dq_compute(const BwdArgs& a, uint32_t sbase, uint32_t tmem,
     tc_fence_after();
     const size_t row = ((size_t)it.b * a.S + (size_t)it.j * kT + r) * a.H + it.h;
     const int e0 = (warp >> 2) * (DH / 2);
-    store_row<DH / 2>(tDQ + e0, a.scale, static_cast<__nv_bfloat16*>(a.dq) + row * DH + e0);
+    store_row<DH / 2>(tDQ + e0, a.scale, static_cast<__nv_bfloat16*>(a.dq) + row * DH + e0,
+                      in_bounds(row * DH + e0, DH / 2, (size_t)a.B * a.S * a.H * DH, a.bounds_trim,
+                                a.status));
     tc_fence_before();
   }
 }

@@ -58,8 +58,13 @@ constexpr int kThreads = 384;
 // setmaxnreg split: ptxas allocates each role's code within its share, so the
 // split decides the spills (200 / 104 left a few in the softmax code; 208 / 88
 // leaves none in the paired kernels and was 0.5-0.9 % faster, bit-identical)
+// The D = 64 kernel for single-tile items keeps 200 / 104: its MMA role spills
+// with fewer than about 104 (800 bytes of reloads at 88, 128 at 104).
 constexpr uint32_t kLaunchRegs = 168, kSoftmaxRegs = 208, kProducerRegs = 88;
+constexpr uint32_t kSoftmaxRegs64Single = 200, kProducerRegs64Single = 104;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kProducerRegs == kThreads * kLaunchRegs,
+              "register split must use exactly the launch allocation");
+static_assert(2 * 128 * kSoftmaxRegs64Single + 128 * kProducerRegs64Single == kThreads * kLaunchRegs,
               "register split must use exactly the launch allocation");
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
@@ -838,6 +843,8 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   const uint32_t tP = SINGLE ? tmem + lane_base + L::S_COL(1) : tS;
   const uint32_t tO = tmem + lane_base + L::O_COL(slot);
   const float c = a.scale_log2;
+  // buffer sizes in elements, for the bounds checks of RA_DEBUG builds
+  const size_t out_n = (size_t)a.B * a.S * a.H * D, lse_n = (size_t)a.B * a.H * a.S;
   uint32_t n = 0;  // S tiles consumed so far by this slot
 
   for (int k = 0;; ++k) {
@@ -853,11 +860,14 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     if (ns == 0 || !needs_tile(a, my_qt, 0)) {
       // block mode only: no key of the block is allowed for these rows
       const int srow = my_qt * kBM + r;
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
-                                             (((size_t)it.b * a.S + srow) * a.H + my_h) * D);
+      const size_t e0 = (((size_t)it.b * a.S + srow) * a.H + my_h) * D;
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + e0);
+      if (in_bounds(e0, D, out_n, a.bounds_trim, a.status)) {
 #pragma unroll 1
-      for (int j = 0; j < D / 8; ++j) orow[j] = make_uint4(0, 0, 0, 0);
-      if (a.lse) a.lse[((size_t)it.b * a.H + my_h) * a.S + srow] = -INFINITY;
+        for (int j = 0; j < D / 8; ++j) orow[j] = make_uint4(0, 0, 0, 0);
+      }
+      const size_t li = ((size_t)it.b * a.H + my_h) * a.S + srow;
+      if (a.lse && in_bounds(li, 1, lse_n, a.bounds_trim, a.status)) a.lse[li] = -INFINITY;
       continue;
     }
     // the slot's last step: the item's last one, or the one before it when
@@ -940,8 +950,9 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
               for (int j = 0; j < 4; ++j) {
                 const int row = 4 * j + (lane >> 3), c = lane & 7;
                 const uint4 v = ld_shared_v4(blk + row * 128 + ((c ^ (row & 7)) << 4));
-                *reinterpret_cast<uint4*>(
-                    obase + (((size_t)it.b * a.S + row0 + 16 * half + row) * a.H + h) * D + c * 8) = v;
+                const size_t e = (((size_t)it.b * a.S + row0 + 16 * half + row) * a.H + h) * D + c * 8;
+                if (in_bounds(e, 8, out_n, a.bounds_trim, a.status))
+                  *reinterpret_cast<uint4*>(obase + e) = v;
               }
             }
           }
@@ -968,13 +979,15 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
             for (int j = 0; j < 8; ++j) {
               const int row = 4 * j + (lane >> 3), c = lane & 7;
               const uint4 v = ld_shared_v4(blk + row * 128 + ((c ^ (row & 7)) << 4));
-              *reinterpret_cast<uint4*>(obase + (((size_t)it.b * a.S + row0 + row) * a.H + h) * D +
-                                        hh * 64 + c * 8) = v;
+              const size_t e = (((size_t)it.b * a.S + row0 + row) * a.H + h) * D + hh * 64 + c * 8;
+              if (in_bounds(e, 8, out_n, a.bounds_trim, a.status))
+                *reinterpret_cast<uint4*>(obase + e) = v;
             }
           }
         } else {
-          uint4* orow = reinterpret_cast<uint4*>(
-              static_cast<__nv_bfloat16*>(a.out) + (((size_t)it.b * a.S + srow) * a.H + h) * D);
+          const size_t e0 = (((size_t)it.b * a.S + srow) * a.H + h) * D;
+          uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + e0);
+          const bool row_ok = in_bounds(e0, D, out_n, a.bounds_trim, a.status);
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
@@ -985,13 +998,13 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
             for (int j = 0; j < 16; ++j)
               w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv_l, __uint_as_float(o[2 * j + 1]) * inv_l);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < 4 && row_ok; ++j)
               orow[c0 / 8 + j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
           }
         }
-        if (a.lse)
-          a.lse[((size_t)it.b * a.H + h) * a.S + srow] =
-              (st.m + log2f(st.l_exact)) * 0.69314718055994531f;
+        const size_t li = ((size_t)it.b * a.H + h) * a.S + srow;
+        if (a.lse && in_bounds(li, 1, lse_n, a.bounds_trim, a.status))
+          a.lse[li] = (st.m + log2f(st.l_exact)) * 0.69314718055994531f;
         tc_fence_before();
       }
     }
@@ -1043,10 +1056,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   if (warp < 8) {
-    regs_inc<kSoftmaxRegs>();
+    regs_inc<(D == 64 && SINGLE) ? kSoftmaxRegs64Single : kSoftmaxRegs>();
     softmax_role<D, SINGLE>(a, sbase, tmem, abort_flag);
   } else {
-    regs_dec<kProducerRegs>();
+    regs_dec<(D == 64 && SINGLE) ? kProducerRegs64Single : kProducerRegs>();
     if (warp == kWarpTma) {
       if ((threadIdx.x & 31) == 0) tma_role<D>(&tm_q, &tm_k, &tm_v, a, sbase, abort_flag);
     } else if (warp == kWarpMma) {

@@ -47,6 +47,8 @@ struct FwdArgs {
   int skip_value_load;   // failure-path test hook
   int mma_order;         // MmaOrder: how S_i(u+1) is ordered after O_i += P_i(u) V
   unsigned int* item_ctr;  // this launch's work-item counter pair (next item, CTAs done), zero at launch
+  long long bounds_trim;   // bounds-checked builds: elements at the end of every buffer that count
+                           // as outside it (test hook; 0 normally)
 };
 
 // Kernel arguments of the backward pass besides the tensor maps (q, k, v, dout).
@@ -70,11 +72,36 @@ struct BwdArgs {
   unsigned long long timeout_ns;
   int skip_first_load;   // failure-path test hook: the dk/dv producer never issues
                          // its first dout-tile copy
+  long long bounds_trim; // as FwdArgs::bounds_trim
 };
 
 // status word bits
 constexpr unsigned int kStatusTimeout = 1u;
 constexpr unsigned int kStatusLayout = 2u;  // a kernel found its shared memory base misaligned
+constexpr unsigned int kStatusBounds = 4u;  // bounds-checked builds: an address outside its buffer
+
+// Builds compiled with RA_DEBUG check every global address a kernel computes
+// (the tensor-map copies are bounded by the hardware) against its buffer:
+// when the element range [first, first + count) does not lie inside
+// [0, extent - trim), the check sets kStatusBounds in the status word and the
+// caller skips the access (a bulk copy reads element 0 instead, so that its
+// barrier still completes).  trim is a test hook that makes the last elements
+// of every buffer count as outside it.  Other builds compile the check away.
+__device__ __forceinline__ bool in_bounds(size_t first, size_t count, size_t extent, long long trim,
+                                          unsigned int* status) {
+#ifdef RA_DEBUG
+  if (extent >= (size_t)trim && first + count <= extent - (size_t)trim) return true;
+  if (status) atomicOr(status, kStatusBounds);
+  return false;
+#else
+  (void)first;
+  (void)count;
+  (void)extent;
+  (void)trim;
+  (void)status;
+  return true;
+#endif
+}
 
 // ra_fwd.cu
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -136,8 +163,9 @@ cudaError_t launch_bwd_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk,
 cudaError_t measure_ceilings(int sms, double* out);
 
 // ra_merge.cu
+// (status, trim: the bounds checks of RA_DEBUG builds)
 cudaError_t launch_merge(const void* o_parts, int o_is_fp32, const float* lse_parts, int n,
                          void* out, float* lse, int B, int H, int S, int D, int sms,
-                         cudaStream_t stream);
+                         unsigned int* status, long long trim, cudaStream_t stream);
 
 }  // namespace ra

@@ -111,12 +111,14 @@ __device__ __forceinline__ float row_weights(float* w, int n, int stride) {
 template <bool kFp32>
 __global__ void __launch_bounds__(kMergeThreads, 2) merge_tiles_kernel(
     const void* __restrict__ o_parts, const float* __restrict__ lse_parts, int n,
-    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int B, int H, int S, int D, int Ts) {
+    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int B, int H, int S, int D, int Ts,
+    unsigned int* status, long long trim) {
   extern __shared__ float w_s[];  // [n][H][Ts]: lse of the tile, then the weights
   const int tiles_per_b = (S + Ts - 1) / Ts;
   const long long n_tiles = (long long)B * tiles_per_b;
   const long long rows = (long long)B * S * H;
   const long long o_stride = rows * D;  // elements per partial
+  const long long lse_n = (long long)B * H * S;  // lse values per partial
   const int vec_per_row = D / 8;
   for (long long tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
     const int b = (int)(tile / tiles_per_b);
@@ -128,7 +130,8 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_tiles_kernel(
       const int j = i % ts;
       const int ph = i / ts;  // p*H + h
       const int p = ph / H, h = ph % H;
-      w_s[i] = __ldg(lse_parts + (((long long)p * B + b) * H + h) * S + s0 + j);
+      const long long li = (((long long)p * B + b) * H + h) * S + s0 + j;
+      w_s[i] = in_bounds(li, 1, n * lse_n, trim, status) ? __ldg(lse_parts + li) : -INFINITY;
     }
     __syncthreads();
     // 2. weights per row (h, j), in place; the row's merged lse
@@ -136,7 +139,8 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_tiles_kernel(
       const float L = row_weights(w_s + r, n, H * ts);
       if (lse) {
         const int h = r / ts, j = r % ts;
-        lse[((long long)b * H + h) * S + s0 + j] = L;
+        const long long li = ((long long)b * H + h) * S + s0 + j;
+        if (in_bounds(li, 1, lse_n, trim, status)) lse[li] = L;
       }
     }
     __syncthreads();
@@ -158,13 +162,17 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_tiles_kernel(
         for (int q = 0; q < kLoadBatch; ++q) {
           const int p = p0 + q;
           wg[q] = p < n ? w_s[p * H * ts + wi] : 0.0f;
-          if (wg[q] != 0.0f) load8<kFp32>(o_parts, p * o_stride + e, x[q]);  // empty: not read
+          // an empty partial (weight 0) is not read
+          if (wg[q] != 0.0f && in_bounds(p * o_stride + e, 8, n * o_stride, trim, status))
+            load8<kFp32>(o_parts, p * o_stride + e, x[q]);
+          else
+            wg[q] = 0.0f;
         }
 #pragma unroll
         for (int q = 0; q < kLoadBatch; ++q)
           if (wg[q] != 0.0f) fma8<kFp32>(acc, wg[q], x[q]);
       }
-      *reinterpret_cast<uint4*>(out + e) = pack8(acc);
+      if (in_bounds(e, 8, o_stride, trim, status)) *reinterpret_cast<uint4*>(out + e) = pack8(acc);
     }
     __syncthreads();  // the weights are rewritten by the next tile
   }
@@ -177,7 +185,8 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(const void* __restrict_
                                                          const float* __restrict__ lse_parts, int n,
                                                          __nv_bfloat16* __restrict__ out,
                                                          float* __restrict__ lse, long long rows,
-                                                         int H, int S, int D) {
+                                                         int H, int S, int D, unsigned int* status,
+                                                         long long trim) {
   const int per_row = D / 8;
   const long long units = rows * per_row;
   const long long o_stride = rows * (long long)D;
@@ -188,24 +197,31 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(const void* __restrict_
     const int h = (int)(row % H);
     const long long bs = row / H;
     const long long li = ((bs / S) * H + h) * S + bs % S;  // [B,H,S] order
+    // a partial outside the buffers (bounds-checked builds only) counts as empty
+    auto lse_of = [&](int p) {
+      return in_bounds(p * rows + li, 1, n * rows, trim, status) ? __ldg(lse_parts + p * rows + li)
+                                                                 : -INFINITY;
+    };
     float M = -INFINITY;
-    for (int p = 0; p < n; ++p) M = fmaxf(M, __ldg(lse_parts + p * rows + li));
+    for (int p = 0; p < n; ++p) M = fmaxf(M, lse_of(p));
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float L = -INFINITY;
     if (M != -INFINITY) {
       float Z = 0.0f;
-      for (int p = 0; p < n; ++p) Z += expf(__ldg(lse_parts + p * rows + li) - M);
+      for (int p = 0; p < n; ++p) Z += expf(lse_of(p) - M);
       L = M + logf(Z);
       for (int p = 0; p < n; ++p) {
-        const float lp = __ldg(lse_parts + p * rows + li);
+        const float lp = lse_of(p);
         if (lp == -INFINITY) continue;
+        if (!in_bounds(p * o_stride + row * D + cpart * 8, 8, n * o_stride, trim, status)) continue;
         Raw8<kFp32> x;
         load8<kFp32>(o_parts, p * o_stride + row * D + cpart * 8, x);
         fma8<kFp32>(acc, expf(lp - L), x);
       }
     }
-    *reinterpret_cast<uint4*>(out + row * D + cpart * 8) = pack8(acc);
-    if (lse && cpart == 0) lse[li] = L;
+    if (in_bounds(row * D + cpart * 8, 8, o_stride, trim, status))
+      *reinterpret_cast<uint4*>(out + row * D + cpart * 8) = pack8(acc);
+    if (lse && cpart == 0 && in_bounds(li, 1, rows, trim, status)) lse[li] = L;
   }
 }
 
@@ -213,7 +229,7 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(const void* __restrict_
 
 cudaError_t launch_merge(const void* o_parts, int o_is_fp32, const float* lse_parts, int n,
                          void* out, float* lse, int B, int H, int S, int D, int sms,
-                         cudaStream_t stream) {
+                         unsigned int* status, long long trim, cudaStream_t stream) {
   auto* o = static_cast<__nv_bfloat16*>(out);
   const long long rows = (long long)B * S * H;
   const long long per_pos = (long long)n * H;  // lse values of one sequence position
@@ -227,10 +243,11 @@ cudaError_t launch_merge(const void* o_parts, int o_is_fp32, const float* lse_pa
     const size_t smem = (size_t)per_pos * Ts * sizeof(float);
     if (o_is_fp32)
       merge_tiles_kernel<true><<<grid, kMergeThreads, smem, stream>>>(o_parts, lse_parts, n, o, lse,
-                                                                    B, H, S, D, Ts);
+                                                                    B, H, S, D, Ts, status, trim);
     else
       merge_tiles_kernel<false><<<grid, kMergeThreads, smem, stream>>>(o_parts, lse_parts, n, o,
-                                                                     lse, B, H, S, D, Ts);
+                                                                     lse, B, H, S, D, Ts, status,
+                                                                     trim);
     return cudaGetLastError();
   }
   const long long units = rows * (D / 8);
@@ -238,10 +255,10 @@ cudaError_t launch_merge(const void* o_parts, int o_is_fp32, const float* lse_pa
   if (grid > (long long)sms * 8) grid = (long long)sms * 8;
   if (o_is_fp32)
     merge_rows_kernel<true><<<(int)grid, 256, 0, stream>>>(o_parts, lse_parts, n, o, lse, rows, H,
-                                                           S, D);
+                                                           S, D, status, trim);
   else
     merge_rows_kernel<false><<<(int)grid, 256, 0, stream>>>(o_parts, lse_parts, n, o, lse, rows, H,
-                                                            S, D);
+                                                            S, D, status, trim);
   return cudaGetLastError();
 }
 
