@@ -276,7 +276,8 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
  * sets a status bit and the access is skipped, with no trap: the next
  * ra_get_last_device_status returns RA_ERR_BOUNDS.  Other builds compile the
  * checks away.
- *   ra_debug_build: 1 in a bounds-checked build, 0 otherwise.
+ *   ra_debug_build: bit 0 set in a bounds-checked build, bit 1 in a traced
+ *     build (below), 0 in the product build.
  *   ra_debug_set_bounds_trim: a test hook for bounds-checked builds; the last
  *     `elements` elements of every checked buffer count as outside it, so a
  *     test can see the checks fire without any access outside a buffer.  0
@@ -285,6 +286,24 @@ void ra_debug_set_fault(long long timeout_ns, int skip_value_load);
  */
 int ra_debug_build(void);
 void ra_debug_set_bounds_trim(long long elements);
+
+/*
+ * Traced builds (a measurement facility, no counterpart on the pages).  The
+ * library compiled with RA_TRACE (libringattn_trace.so, built by
+ * `python -m ring_chunked_attention_gb300.build --trace`; the binding loads it
+ * when the environment variable RA_TRACE is 1) counts clock cycles per role
+ * in every CTA of the forward kernel: where its MMA warp, softmax warps and
+ * producer thread wait or work.  Each CTA stores 32 counters when its roles
+ * end (a launch first zeroes them all, so slots of CTAs it did not run read
+ * 0); ra_trace_read synchronises the device and copies the counters of the
+ * last forward launch's first n_ctas CTAs (at most 1024) into out
+ * (n_ctas * 32 values, host memory).  The slot layout is given with
+ * `python -m ring_chunked_attention_gb300.trace`, which runs a workload and
+ * prints the per-step breakdown.  Returns RA_ERR_UNSUPPORTED in other builds,
+ * RA_ERR_INVALID_ARG for a NULL out or n_ctas <= 0, RA_ERR_CUDA if the copy
+ * fails.
+ */
+ra_status ra_trace_read(unsigned long long* out, int n_ctas);
 
 /*
  * MMA issue order of ra_fwd and ra_fwd_block (no counterpart on the pages; an

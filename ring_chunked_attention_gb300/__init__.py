@@ -25,20 +25,25 @@ __all__ = ["ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspac
            "RaError", "library_path", "MMA_ORDER_GROUPED", "MMA_ORDER_STRICT", "MMA_ORDER_INORDER",
            "MMA_ORDER_BRIDGED",
            "RA_OK", "RA_ERR_INVALID_ARG", "RA_ERR_UNSUPPORTED", "RA_ERR_CUDA", "RA_ERR_TIMEOUT",
-           "RA_ERR_BOUNDS", "ra_debug_build", "ra_debug_set_bounds_trim"]
+           "RA_ERR_BOUNDS", "ra_debug_build", "ra_debug_set_bounds_trim", "ra_trace_build",
+           "ra_trace_read"]
 
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT, RA_ERR_BOUNDS = (
     0, 1, 2, 3, 4, 5)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-# RA_DEBUG=1 selects the bounds-checked build (python -m ring_chunked_attention_gb300.build --debug)
+# RA_DEBUG=1 selects the bounds-checked build (python -m ring_chunked_attention_gb300.build --debug),
+# RA_TRACE=1 the traced one (--trace)
 _DEBUG = os.environ.get("RA_DEBUG", "0") == "1"
-_LIB_PATH = os.path.join(_HERE, "libringattn_debug.so" if _DEBUG else "libringattn.so")
+_TRACE = os.environ.get("RA_TRACE", "0") == "1" and not _DEBUG
+_LIB_PATH = os.path.join(_HERE, "libringattn_debug.so" if _DEBUG else
+                         "libringattn_trace.so" if _TRACE else "libringattn.so")
 _lib = None
 
 EXPORTS = ("ra_fwd", "ra_fwd_block", "ra_bwd", "ra_bwd_static", "ra_bwd_workspace_bytes", "ra_merge_partials", "ra_measure_ceilings", "ra_get_last_device_status", "ra_status_string",
            "ra_last_cuda_error", "ra_version", "ra_debug_set_fault", "ra_set_mma_order",
-           "ra_set_item_pairing", "ra_shutdown", "ra_debug_build", "ra_debug_set_bounds_trim")
+           "ra_set_item_pairing", "ra_shutdown", "ra_debug_build", "ra_debug_set_bounds_trim",
+           "ra_trace_read")
 
 
 class RaError(RuntimeError):
@@ -59,7 +64,7 @@ def _load():
     if not os.path.exists(_LIB_PATH):
         raise RuntimeError(f"{os.path.basename(_LIB_PATH)} is not built ({_LIB_PATH}); run "
                            "`python -m ring_chunked_attention_gb300.build`"
-                           + (" --debug" if _DEBUG else ""))
+                           + (" --debug" if _DEBUG else " --trace" if _TRACE else ""))
     lib = ctypes.CDLL(_LIB_PATH)
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.ra_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
@@ -98,6 +103,8 @@ def _load():
     lib.ra_debug_build.restype = i
     lib.ra_debug_set_bounds_trim.argtypes = [ctypes.c_longlong]
     lib.ra_debug_set_bounds_trim.restype = None
+    lib.ra_trace_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i]
+    lib.ra_trace_read.restype = i
     _lib = lib
     return lib
 
@@ -362,7 +369,22 @@ def ra_set_mma_order(order: int) -> None:
 
 def ra_debug_build() -> bool:
     """True when the loaded library is the bounds-checked build."""
-    return bool(_load().ra_debug_build())
+    return bool(_load().ra_debug_build() & 1)
+
+
+def ra_trace_build() -> bool:
+    """True when the loaded library is the traced build."""
+    return bool(_load().ra_debug_build() & 2)
+
+
+def ra_trace_read(n_ctas: int = 152):
+    """Per-role cycle counters of the last forward launch (traced builds):
+    an int64 tensor [n_ctas, 32]; see ring_chunked_attention_gb300.trace."""
+    import torch
+
+    buf = (ctypes.c_ulonglong * (32 * n_ctas))()
+    _check(_load().ra_trace_read(buf, int(n_ctas)), "ra_trace_read")
+    return torch.tensor(list(buf), dtype=torch.int64).view(n_ctas, 32)
 
 
 def ra_debug_set_bounds_trim(elements: int) -> None:

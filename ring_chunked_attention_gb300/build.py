@@ -6,7 +6,8 @@ The result lands beside this file (git-ignored).  Run as a script or call
 flavour instead, ``libringattn_debug.so`` (compiled with ``RA_DEBUG``: every
 global address a kernel computes is checked against its buffer; see
 ``include/ringattn.h``), which the binding loads when the environment variable
-``RA_DEBUG`` is ``1``.
+``RA_DEBUG`` is ``1``; ``--trace`` builds ``libringattn_trace.so`` (``RA_TRACE``:
+per-role cycle counters in the forward kernel), loaded when ``RA_TRACE`` is ``1``.
 """
 from __future__ import annotations
 
@@ -23,6 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libringattn.so")
 DEBUG_LIB = os.path.join(HERE, "libringattn_debug.so")
+TRACE_LIB = os.path.join(HERE, "libringattn_trace.so")
 SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_merge.cu", "ra_ceil.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -49,14 +51,17 @@ def _stale(lib: str) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
-          debug: bool = False) -> str:
-    lib = DEBUG_LIB if debug else LIB
+          debug: bool = False, trace: bool = False) -> str:
+    if debug and trace:
+        raise ValueError("one flavour at a time: debug or trace")
+    lib = DEBUG_LIB if debug else TRACE_LIB if trace else LIB
     if not force and not _stale(lib):
         return lib
     nvcc = _nvcc()
-    build_dir = BUILD_DIR + ("_debug" if debug else "")
+    build_dir = BUILD_DIR + ("_debug" if debug else "_trace" if trace else "")
     os.makedirs(build_dir, exist_ok=True)
-    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DRA_DEBUG"] if debug else [])
+    extra = ((["-Xptxas", "-v"] if ptxas_info else []) + (["-DRA_DEBUG"] if debug else [])
+             + (["-DRA_TRACE"] if trace else []))
 
     def compile_one(src):
         obj = os.path.join(build_dir, src.replace(".cu", ".o"))
@@ -83,4 +88,4 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True, ptxas_info="-v" in sys.argv,
-                debug="--debug" in sys.argv))
+                debug="--debug" in sys.argv, trace="--trace" in sys.argv))

@@ -497,12 +497,30 @@ void ra_debug_set_bounds_trim(long long elements) {
   g_bounds_trim = elements > 0 ? elements : 0;
 }
 
-int ra_debug_build(void) {
-#ifdef RA_DEBUG
-  return 1;
+ra_status ra_trace_read(unsigned long long* out, int n_ctas) {
+#ifdef RA_TRACE
+  if (!out || n_ctas <= 0) return RA_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = ra::trace_copy(out, n_ctas);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return RA_OK;
 #else
-  return 0;
+  (void)out;
+  (void)n_ctas;
+  return RA_ERR_UNSUPPORTED;
 #endif
+}
+
+int ra_debug_build(void) {
+  int flags = 0;
+#ifdef RA_DEBUG
+  flags |= 1;
+#endif
+#ifdef RA_TRACE
+  flags |= 2;
+#endif
+  return flags;
 }
 
 void ra_set_mma_order(int order) {

@@ -51,6 +51,21 @@
 namespace ra {
 
 __device__ unsigned int g_status_word;
+#ifdef RA_TRACE
+__device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
+#endif
+
+// RA_TRACE builds: one role's counters into this CTA's trace slots (lane 0)
+__device__ __forceinline__ void trace_store(const unsigned long long* arr, int n, int first) {
+#ifdef RA_TRACE
+  if ((threadIdx.x & 31) == 0 && blockIdx.x < kTraceCtas)
+    for (int i = 0; i < n; ++i) g_trace[blockIdx.x * kTraceSlots + first + i] = arr[i];
+#else
+  (void)arr;
+  (void)n;
+  (void)first;
+#endif
+}
 // work-item counters: per slot the next unclaimed item and the CTAs done
 __device__ unsigned int g_item_ctr[2 * kItemCounterSlots];
 
@@ -301,6 +316,7 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
   // fewer items.
   const int first_claimed = (int)gridDim.x;
   int claim = (int)blockIdx.x;
+  RA_TR_DECL(tr, 3);
   for (int k = 0; ok; ++k) {
     const int x = claim;
     const int rs = k % kItemRing;
@@ -333,11 +349,13 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 #pragma unroll
     for (int slot = 0; slot < 2 && ok; ++slot) {
       if (slot == 1 && !it.valid1) continue;
+      RA_TR_NOW(tr_q);
       if (q_cnt[slot] > 0 &&
           !wait_bounded(bar(L::Q_EMPTY + slot), (q_cnt[slot] - 1) & 1, abort_flag, a)) {
         ok = false;
         break;
       }
+      RA_TR_ADD(tr, 2, tr_q);
       if (slot == 0) st_shared_i32(sbase + L::QID_OFF, x);  // released by the arrive below
       mbar_arrive_expect_tx(bar(L::Q_FULL + slot), L::TILE);
       for (int kb = 0; kb < L::DK; ++kb)
@@ -353,13 +371,17 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
       const uint32_t ph = (kv_cnt / L::NS) & 1;
       const int row = it.b * a.Sk + kt * kBN;
       if (u == ns - 1) claim = first_claimed + (int)atomicAdd(a.item_ctr, 1u);  // the next item
+      RA_TR_NOW(tr_k);
       if (!wait_bounded(bar(L::K_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
+      RA_TR_ADD(tr, 0, tr_k);
       mbar_arrive_expect_tx(bar(L::K_FULL + st), L::TILE);
       for (int kb = 0; kb < L::DK; ++kb)
         tma_load_3d(sbase + L::K_OFF + st * L::TILE + kb * L::BLOCK, tk, bar(L::K_FULL + st),
                     kb * 64, it.kvh, row, pol_kv);
       ++k_cnt;
+      RA_TR_NOW(tr_v);
       if (!wait_bounded(bar(L::V_EMPTY + st), ph ^ 1, abort_flag, a)) { ok = false; break; }
+      RA_TR_ADD(tr, 1, tr_v);
       mbar_arrive_expect_tx(bar(L::V_FULL + st), L::TILE);
       if (!(a.skip_value_load && kv_cnt == 0))
         for (int kb = 0; kb < L::DK; ++kb)
@@ -368,6 +390,9 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
       ++kv_cnt;
     }
   }
+#ifdef RA_TRACE
+  trace_store(tr, 3, 28);
+#endif
   // the last claim has returned (its value is used here) before this CTA can
   // count itself done and the last CTA resets the counter
   asm volatile("" ::"r"(claim));
@@ -478,8 +503,11 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   uint32_t q_cnt0 = 0, q_cnt1 = 0;
   uint32_t c = 0;                   // ring position of the current step
   bool ok = true;
+  RA_TR_DECL(tr, 10);
+  RA_TR_NOW(tr_begin);
 
   while (ok) {
+    RA_TR_NOW(tr_item);
     // the next item with work: its id comes with its first query tile (-1: none left)
     if (!wait_all(bar(L::Q_FULL + 0), q_cnt0 & 1, abort_flag, a)) break;
     ++q_cnt0;
@@ -522,6 +550,8 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       }
     }
     bool first0 = true, first1 = true;
+    RA_TR_ADD(tr, 7, tr_item);
+    RA_TR_INC(tr, 9);
     for (int u = 0; u < ns && ok; ++u, ++c) {
       const int st = c % L::NS;
       const bool n0 = nxt.kt <= lim0, n1 = nxt.kt <= lim1;
@@ -529,7 +559,13 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (more) nxt.next();
       const bool m0 = more && nxt.kt <= lim0, m1 = more && nxt.kt <= lim1;
       const int st1 = (c + 1) % L::NS;
+      RA_TR_NOW(tr_w);
       if (!wait_all(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+      RA_TR_ADD(tr, 2, tr_w);
+#ifdef RA_TRACE
+      if (u == 0) RA_TR_ADD(tr, 8, tr_w);
+#endif
+      RA_TR_INC(tr, 4);
       // K(u+1) is needed only by the next S products.  At D = 128 (a 2-deep
       // ring) it is waited for after slot 0's PV, which gives its copy that much
       // longer to land: GQA 2.72 against 2.81 ms.  At D = 64 the 5-deep ring has
@@ -545,17 +581,25 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (ORDER == MMA_ORDER_GROUPED) {
         // both PV products, then each slot's next S once its PV has completed
         if (n0) {
+          RA_TR_NOW(tr_p);
           if (!wait_all(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          RA_TR_ADD(tr, 0, tr_p);
+          RA_TR_NOW(tr_i);
           tc_fence_after();
           issue_pv<D>(tO0, tP0, v_desc(st), !first0);
           mma_commit_e(bar(L::O_FREE + 0));
+          RA_TR_ADD(tr, 1, tr_i);
           first0 = false;
         }
         if (n1) {
+          RA_TR_NOW(tr_p);
           if (!wait_all(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          RA_TR_ADD(tr, 0, tr_p);
+          RA_TR_NOW(tr_i);
           tc_fence_after();
           issue_pv<D>(tO1, tS1, v_desc(st), !first1);
           mma_commit_e(bar(L::O_FREE + 1));
+          RA_TR_ADD(tr, 1, tr_i);
           first1 = false;
         }
         mma_commit_e(bar(L::V_EMPTY + st));
@@ -580,40 +624,54 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       } else {
         // slot 0: PV(u), then S(u+1)
         if (n0) {
+          RA_TR_NOW(tr_p);
           if (!wait_all(bar(L::P_FULL + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          RA_TR_ADD(tr, 0, tr_p);
+          RA_TR_NOW(tr_i);
           tc_fence_after();
           issue_pv<D>(tO0, tP0, v_desc(st), !first0);
           mma_commit_e(bar(L::O_FREE + 0));
+          RA_TR_ADD(tr, 1, tr_i);
           first0 = false;
         }
         if (more && !k_ready) {
+          RA_TR_NOW(tr_k);
           if (!wait_all(bar(L::K_FULL + st1), ((c + 1) / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+          RA_TR_ADD(tr, 6, tr_k);
           k_ready = true;
         }
         if (m0) {
+          RA_TR_NOW(tr_s);
           if (ORDER == MMA_ORDER_BRIDGED && !P_APART) tmem_shift_down_e(tS0 + 64u);
           if (ORDER == MMA_ORDER_STRICT && !P_APART &&
               !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
           mma_commit_e(bar(L::S_FULL + 0));
+          RA_TR_ADD(tr, 3, tr_s);
           ++s_cnt0;
         }
         // slot 1: PV(u), then S(u+1)
         if (n1) {
+          RA_TR_NOW(tr_p);
           if (!wait_all(bar(L::P_FULL + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          RA_TR_ADD(tr, 0, tr_p);
+          RA_TR_NOW(tr_i);
           tc_fence_after();
           issue_pv<D>(tO1, tS1, v_desc(st), !first1);
           mma_commit_e(bar(L::O_FREE + 1));
+          RA_TR_ADD(tr, 1, tr_i);
           first1 = false;
         }
         if (m1) {
+          RA_TR_NOW(tr_s);
           if (ORDER == MMA_ORDER_BRIDGED) tmem_shift_down_e(tS1 + 64u);
           if (ORDER == MMA_ORDER_STRICT && s_cnt1 > 0 &&
               !wait_all(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);
           mma_commit_e(bar(L::S_FULL + 1));
+          RA_TR_ADD(tr, 3, tr_s);
           ++s_cnt1;
         }
         mma_commit_e(bar(L::V_EMPTY + st));
@@ -625,6 +683,11 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       }
     }
   }
+#ifdef RA_TRACE
+  RA_TR_ADD(tr, 5, tr_begin);
+  trace_store(tr, 8, 0);
+  trace_store(tr + 8, 2, 24);
+#endif
   // Every MMA this thread issued completes before tensor memory is freed.
   mma_commit_e(bar(L::DONE));
   wait_drain(bar(L::DONE), 0, a.timeout_ns);
@@ -846,6 +909,7 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   // buffer sizes in elements, for the bounds checks of RA_DEBUG builds
   const size_t out_n = (size_t)a.B * a.S * a.H * D, lse_n = (size_t)a.B * a.H * a.S;
   uint32_t n = 0;  // S tiles consumed so far by this slot
+  RA_TR_DECL(tr, 6);
 
   for (int k = 0;; ++k) {
     const int x = next_item<D>(a, sbase, k, abort_flag);
@@ -882,7 +946,10 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     for (int u = 0; u < ns; ++u, cur.next()) {
       const int kt = cur.kt;
       if (!needs_tile(a, my_qt, kt)) continue;
+      RA_TR_NOW(tr_0);
       if (!wait_all(bar(L::S_FULL + slot), n & 1, abort_flag, a)) return;
+      RA_TR_ADD(tr, 0, tr_0);
+      RA_TR_NOW(tr_1);
       tc_fence_after();
       PackedRow pk;
       if (is_diag(a, my_qt, kt))
@@ -892,14 +959,19 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       tc_fence_before();
       __syncwarp();
       mbar_arrive_e(bar(L::P_FULL + slot));
+      RA_TR_ADD(tr, 1, tr_1);
+      RA_TR_NOW(tr_2);
       // the sum of the rounded weights is needed only by the epilogue: taken
       // here, while the tensor cores run this slot's PV and next S products
       // (with the row-sum columns the PV product sums them itself)
       if (!SoftmaxPolicy<D>::kMmaRowSum) st.l_round += rounded_sum(pk);
       ++n;
       first = false;
+      RA_TR_ADD(tr, 2, tr_2);
+      RA_TR_INC(tr, 3);
 
       if (u == u_last) {
+        RA_TR_NOW(tr_e);
         // epilogue: wait for the last O_i += P_i V, then out = O / l, lse
         if (!wait_all(bar(L::O_FREE + slot), (n - 1) & 1, abort_flag, a)) return;
         tc_fence_after();
@@ -1006,6 +1078,11 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         if (a.lse && in_bounds(li, 1, lse_n, a.bounds_trim, a.status))
           a.lse[li] = (st.m + log2f(st.l_exact)) * 0.69314718055994531f;
         tc_fence_before();
+#ifdef RA_TRACE
+        RA_TR_ADD(tr, 4, tr_e);
+        RA_TR_INC(tr, 5);
+        if ((warp & 3) == 0) trace_store(tr, 6, slot ? 16 : 8);
+#endif
       }
     }
   }
@@ -1107,6 +1184,14 @@ static cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const 
   static std::atomic<unsigned> prepared[kMaxPrepDevices];
   const cudaError_t e = prepare_kernel(ring_attn_fwd_kernel<D, SINGLE>, (int)kLaunchRegs, smem, prepared);
   if (e != cudaSuccess) return e;
+#ifdef RA_TRACE
+  {  // traced builds: the counters describe this launch alone
+    void* tr = nullptr;
+    cudaError_t te = cudaGetSymbolAddress(&tr, g_trace);
+    if (te == cudaSuccess) te = cudaMemsetAsync(tr, 0, sizeof(g_trace), stream);
+    if (te != cudaSuccess) return te;
+  }
+#endif
   ring_attn_fwd_kernel<D, SINGLE><<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }
@@ -1123,6 +1208,17 @@ cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
 
 cudaError_t item_counter_ptr(unsigned int** p) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_item_ctr);
+}
+
+cudaError_t trace_copy(unsigned long long* host, int n_ctas) {
+#ifdef RA_TRACE
+  if (n_ctas > kTraceCtas) n_ctas = kTraceCtas;
+  return cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * kTraceSlots * n_ctas);
+#else
+  (void)host;
+  (void)n_ctas;
+  return cudaErrorNotSupported;
+#endif
 }
 
 cudaError_t status_word_ptr(unsigned int** p) {

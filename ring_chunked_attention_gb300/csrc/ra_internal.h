@@ -103,6 +103,30 @@ __device__ __forceinline__ bool in_bounds(size_t first, size_t count, size_t ext
 #endif
 }
 
+// Per-role cycle counters of builds compiled with RA_TRACE (ra_trace_read):
+// each CTA of the forward kernel keeps kTraceSlots clock64 sums in registers
+// and stores them when its roles finish.  Other builds compile the counting
+// away.  Slots: MMA warp 0 P waits, 1 PV issue, 2 V waits, 3 S issue,
+// 4 steps, 5 role total, 6 late K waits, 7 item starts (Q waits and the first
+// S); softmax slot 0 warp 0 at 8.., slot 1 (warp 4) at 16..: +0 S waits,
+// +1 S to P hand-off, +2 after the hand-off, +3 tiles, +4 epilogues, +5 items;
+// 24 V waits at an item's first step, 25 items (MMA warp); producer 28 K-stage
+// waits, 29 V-stage waits, 30 Q-slot waits.
+constexpr int kTraceSlots = 32;
+constexpr int kTraceCtas = 1024;
+#ifdef RA_TRACE
+#define RA_TR_DECL(name, n) unsigned long long name[n] = {}
+#define RA_TR_NOW(v) const long long v = clock64()
+#define RA_TR_ADD(arr, i, v) ((arr)[i] += (unsigned long long)(clock64() - (v)))
+#define RA_TR_INC(arr, i) ((arr)[i] += 1ull)
+#else
+#define RA_TR_DECL(name, n)
+#define RA_TR_NOW(v)
+#define RA_TR_ADD(arr, i, v)
+#define RA_TR_INC(arr, i)
+#endif
+cudaError_t trace_copy(unsigned long long* host, int n_ctas);
+
 // ra_fwd.cu
 cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& args, int grid, cudaStream_t stream);

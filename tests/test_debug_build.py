@@ -1,18 +1,27 @@
-"""The bounds-checked flavour of the library (RA_DEBUG) builds here without a
-GPU, exports the same C ABI and says that it is the checked build; the
-product build says it is not.  (Its kernels run in tests/test_debug_gpu.py.)"""
+"""The checked (RA_DEBUG) and traced (RA_TRACE) flavours of the library build
+here without a GPU, export the same C ABI and say which flavour they are; the
+product build says it is neither and refuses ra_trace_read.  (Their kernels
+run in tests/test_debug_gpu.py and tests/test_trace_gpu.py.)"""
 import ctypes
+
+import pytest
 
 from tests.test_capi import _declared_functions
 
 
-def test_debug_flavour_builds_and_reports_itself(ralib):
+@pytest.mark.parametrize("flavour,flag", [("debug", 1), ("trace", 2)])
+def test_flavour_builds_and_reports_itself(ralib, flavour, flag):
     from ring_chunked_attention_gb300 import build as rab
 
-    path = rab.build(debug=True)
-    dbg = ctypes.CDLL(path)
-    missing = [n for n in _declared_functions() if not hasattr(dbg, n)]
+    path = rab.build(**{flavour: True})
+    lib = ctypes.CDLL(path)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
     assert not missing, f"not exported: {missing}"
-    assert dbg.ra_debug_build() == 1
+    assert lib.ra_debug_build() == flag
+
+
+def test_product_build_is_neither(ralib):
     assert ctypes.CDLL(ralib.library_path()).ra_debug_build() == 0
     assert ralib.ra_status_string(ralib.RA_ERR_BOUNDS) == "RA_ERR_BOUNDS"
+    buf = (ctypes.c_ulonglong * 32)()
+    assert ralib._load().ra_trace_read(buf, 1) == ralib.RA_ERR_UNSUPPORTED

@@ -414,3 +414,37 @@ def test_mma_orders_are_bit_identical(ralib, cuda_ok, name):
         ralib.ra_set_item_pairing(0)
     for o, l in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+def test_bridged_order_under_contention(ralib, cuda_ok):
+    """The default order relies on tcgen05.mma -> tcgen05.shift -> tcgen05.mma
+    executing in issue order; any hazard would depend on timing.  Paired and
+    single-tile launches of three shapes (D = 128 and 64) run together on four
+    streams, several rounds, so that CTAs of different launches share SMs and
+    the copy engines and L2 are contended; every result must equal the same
+    call made alone under the commit-wait order."""
+    shapes = [Workload("c1", 2, 8, 2, 2048, 128, 4, True), Workload("c2", 1, 6, 3, 1536, 64, 3, True),
+              Workload("c3", 1, 4, 4, 1024, 128, 2, False)]
+    ins = [tuple(t.cuda() for t in make_inputs(w, seed=61 + i)) for i, w in enumerate(shapes)]
+    ralib.ra_set_mma_order(ralib.MMA_ORDER_STRICT)
+    try:
+        refs = [ralib.ra_fwd(*x, P=w.P, causal=w.causal) for x, w in zip(ins, shapes)]
+        torch.cuda.synchronize()
+    finally:
+        ralib.ra_set_mma_order(ralib.MMA_ORDER_BRIDGED)
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    jobs = [(i % len(shapes), streams[i]) for i in range(4)]
+    outs = [(torch.empty_like(refs[j][0]), torch.empty_like(refs[j][1])) for j, _ in jobs]
+    for rnd in range(6):
+        ralib.ra_set_item_pairing(rnd % 3)
+        try:
+            for (j, s), (o, l) in zip(jobs, outs):
+                with torch.cuda.stream(s):
+                    ralib.ra_fwd(*ins[j], P=shapes[j].P, causal=shapes[j].causal, out=o, lse=l,
+                                 stream=s)
+            torch.cuda.synchronize()
+        finally:
+            ralib.ra_set_item_pairing(0)
+        assert ralib.ra_get_last_device_status() == ralib.RA_OK
+        for (j, _), (o, l) in zip(jobs, outs):
+            assert torch.equal(o, refs[j][0]) and torch.equal(l, refs[j][1]), (rnd, j)
