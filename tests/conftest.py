@@ -22,12 +22,16 @@ def oracle_mod():
 
 @pytest.fixture(scope="session")
 def ralib():
-    """The built libringattn (compiled in-tree on first use)."""
+    """The built libringattn (compiled in-tree on first use): the product
+    build, or the bounds-checked / traced flavour when RA_DEBUG / RA_TRACE is
+    1 (the binding loads that one)."""
     from ring_chunked_attention_gb300 import build as b
 
     b.build()
     import ring_chunked_attention_gb300 as ra
 
+    if ra._DEBUG or ra._TRACE:
+        b.build(debug=ra._DEBUG, trace=ra._TRACE)
     ra._load()
     return ra
 

@@ -21,7 +21,11 @@ def test_flavour_builds_and_reports_itself(ralib, flavour, flag):
 
 
 def test_product_build_is_neither(ralib):
-    assert ctypes.CDLL(ralib.library_path()).ra_debug_build() == 0
+    from ring_chunked_attention_gb300 import build as rab
+
+    prod = ctypes.CDLL(rab.LIB)
+    assert prod.ra_debug_build() == 0
     assert ralib.ra_status_string(ralib.RA_ERR_BOUNDS) == "RA_ERR_BOUNDS"
     buf = (ctypes.c_ulonglong * 32)()
-    assert ralib._load().ra_trace_read(buf, 1) == ralib.RA_ERR_UNSUPPORTED
+    prod.ra_trace_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]
+    assert prod.ra_trace_read(buf, 1) == ralib.RA_ERR_UNSUPPORTED
