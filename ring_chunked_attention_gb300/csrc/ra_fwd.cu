@@ -141,6 +141,10 @@ struct Layout {
   static constexpr int BYTES = QID_OFF + 4;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
   __host__ __device__ static constexpr uint32_t S_COL(int i) { return 128u * i; }
+  // one query tile per item: S double-buffered (its second buffer in slot 1's
+  // O columns) and P double-buffered in slot 1's S columns
+  __host__ __device__ static constexpr uint32_t S1T_S_COL(uint32_t i) { return i ? 384u : 0u; }
+  __host__ __device__ static constexpr uint32_t S1T_P_COL(uint32_t i) { return 128u + 64u * i; }
   __host__ __device__ static constexpr uint32_t O_COL(int i) { return 256u + (uint32_t)OW * i; }
 };
 
@@ -476,6 +480,98 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo
   for (int kk = 0; kk < kBN / 16; ++kk)
     mma_ts_lh_e(tO, tP + kk * 8, v_lo + (uint32_t)(kk * (2048 >> 4)), kDescHiSw128, idesc_pv,
               (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// One query tile per item (slot 1 idle): S runs two steps ahead of PV.  The
+// n-th S goes to buffer n % 2 and the softmax writes the n-th P to P buffer
+// n % 2, so S(u+2) can start as soon as the softmax has handed over P(u), and
+// the tensor cores compute it while the softmax works on S(u+1).  The slot's
+// two S_FULL and two P_FULL barriers are one per buffer (a softmax warp can be
+// a tile ahead of its warpgroup, never two).  Orders:
+// S(u+2) rewrites S buffer u % 2 after PV(u) was issued and after P_FULL(u)
+// (the softmax is done with S(u)); P(u+2) is written after S_FULL(u+2), whose
+// commit follows PV(u); the softmax's rare O rescale at tile u+1 waits for
+// the O_FREE commit of PV(u) itself.
+template <int D>
+__device__ void mma_role_single(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
+                                volatile int* abort_flag) {
+  using L = Layout<D>;
+  auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
+  const uint32_t tO0 = tmem + L::O_COL(0);
+  const uint32_t q_lo0 = desc_lo(sbase + L::Q_OFF, 16);
+  const uint32_t k_lo0 = desc_lo(sbase + L::K_OFF, 16);
+  const uint32_t v_lo0 = desc_lo(sbase + L::V_OFF, L::kRowSum ? (uint32_t)(L::ONES_OFF - L::V_OFF) : L::BLOCK);
+  constexpr uint32_t kStageLo = (uint32_t)L::TILE >> 4;
+  auto v_desc = [&](int st) -> uint32_t {
+    return L::kRowSum ? v_lo0 + st * kStageLo - ((st * kStageLo) << 16) : v_lo0 + st * kStageLo;
+  };
+  uint32_t s_cnt = 0;  // S products issued (the n-th into S buffer n % 2)
+  uint32_t p_cnt = 0;  // PV products issued (the n-th reads P buffer n % 2)
+  uint32_t q_cnt = 0;
+  uint32_t c = 0;      // ring position of the current step
+  bool ok = true;
+  while (ok) {
+    if (!wait_all(bar(L::Q_FULL + 0), q_cnt & 1, abort_flag, a)) break;
+    ++q_cnt;
+    const int x = ld_shared_i32(sbase + L::QID_OFF);
+    if (x < 0) break;
+    const Item it = decode_item(a, x);
+    const int ns = n_steps(a, it);
+    const int lim0 = a.causal ? a.q_tile0 + it.qt[0] - a.k_tile0 : INT_MAX;
+    StepCursor cs;  // the step whose S is issued next
+    cs.init(a, it);
+    // S of the step cs points at, from K at ring position cpos
+    auto issue_next_s = [&](uint32_t cpos) -> bool {
+      const int st = cpos % L::NS;
+      if (!wait_all(bar(L::K_FULL + st), (cpos / L::NS) & 1, abort_flag, a)) return false;
+      if (cs.kt <= lim0) {
+        const uint32_t buf = s_cnt & 1u;
+        tc_fence_after();
+        issue_s<D>(tmem + L::S1T_S_COL(buf), q_lo0, k_lo0 + st * kStageLo);
+        mma_commit_e(bar(L::S_FULL + (int)buf));
+        ++s_cnt;
+      }
+      mma_commit_e(bar(L::K_EMPTY + st));
+      return true;
+    };
+    // prologue: S of steps 0 and 1
+    if (!issue_next_s(c)) break;
+    if (ns > 1) {
+      cs.next();
+      if (!issue_next_s(c + 1)) break;
+    }
+    if (ns <= 2) mma_commit_e(bar(L::Q_EMPTY + 0));  // the item's last S is issued
+    StepCursor cp;  // the step whose PV is issued now
+    cp.init(a, it);
+    bool first = true;
+    for (int u = 0; u < ns && ok; ++u, ++c, cp.next()) {
+      const int st = c % L::NS;
+      if (!wait_all(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+      if (cp.kt <= lim0) {
+        // P_FULL per P buffer: a softmax warp may run a tile ahead of the
+        // others (its next S is already there), so the arrivals of tile n and
+        // n + 1 go to different barriers
+        if (!wait_all(bar(L::P_FULL + (int)(p_cnt & 1u)), (p_cnt >> 1) & 1u, abort_flag, a)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv<D>(tO0, tmem + L::S1T_P_COL(p_cnt & 1u), v_desc(st), !first);
+        mma_commit_e(bar(L::O_FREE + 0));
+        ++p_cnt;
+        first = false;
+      }
+      mma_commit_e(bar(L::V_EMPTY + st));
+      if (u + 2 < ns) {
+        cs.next();
+        if (!issue_next_s(c + 2)) { ok = false; break; }
+        if (u + 3 == ns) mma_commit_e(bar(L::Q_EMPTY + 0));
+      }
+    }
+  }
+  // Every MMA this thread issued completes before tensor memory is freed.
+  mma_commit_e(bar(L::DONE));
+  wait_drain(bar(L::DONE), 0, a.timeout_ns);
 }
 
 template <int D, int ORDER, bool P_APART>
@@ -831,9 +927,13 @@ __device__ __forceinline__ float row_max(const uint32_t (&va)[32], const uint32_
 // read again from tensor memory (P is stored only once the weights are
 // accepted): row max, new reference where the max passed m + threshold, O
 // rescale, exps again.
+// pv_bar: the O_FREE barrier and the parity of the previous PV's commit, or
+// 0 when every earlier PV is known complete (its commit preceded this S's)
 template <int D, bool DIAG>
-__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tP, uint32_t tO, int r, float c,
-                                             bool first, RowState& st, PackedRow& pk) {
+__device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tP, uint32_t tO, int r, float c,
+                                             bool first, RowState& st, PackedRow& pk,
+                                             uint32_t pv_bar, uint32_t pv_parity,
+                                             volatile int* abort_flag, const FwdArgs& a) {
   constexpr float kSpecLimit = 1073741824.0f;  // 2^30
   float se;
   {
@@ -884,7 +984,12 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tP, uint32_t 
       st.l_exact *= alpha;
       st.l_round *= alpha;
     }
-    if (__any_sync(0xffffffffu, alpha != 1.0f)) rescale_o<D>(tO, alpha);
+    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+      // O holds the previous PV's result once its commit has arrived
+      if (pv_bar != 0u && !wait_all(pv_bar, pv_parity, abort_flag, a)) return false;
+      tc_fence_after();
+      rescale_o<D>(tO, alpha);
+    }
     const uint64_t c2 = f2_pack(c, c);
     const uint64_t negm2 = f2_pack(-st.m, -st.m);
     uint64_t se0 = 0, se1 = 0;
@@ -904,6 +1009,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tP, uint32_t 
   tmem_st16(tP + 48, pk.d);
   st.l_exact += se;
   tmem_wait_st();
+  return true;
 }
 
 template <int D, bool SINGLE>
@@ -915,9 +1021,7 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   const int slot = warp >> 2;
   const int r = threadIdx.x & 127;  // row inside the 128-row query tile == TMEM lane
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-  const uint32_t tS = tmem + lane_base + L::S_COL(slot);
-  // one query tile per item: P goes to the unused slot's S columns, apart from S
-  const uint32_t tP = SINGLE ? tmem + lane_base + L::S_COL(1) : tS;
+  const uint32_t tS_pair = tmem + lane_base + L::S_COL(slot);
   const uint32_t tO = tmem + lane_base + L::O_COL(slot);
   const float c = a.scale_log2;
   // buffer sizes in elements, for the bounds checks of RA_DEBUG builds
@@ -961,18 +1065,36 @@ __device__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       const int kt = cur.kt;
       if (!needs_tile(a, my_qt, kt)) continue;
       RA_TR_NOW(tr_0);
-      if (!wait_all(bar(L::S_FULL + slot), n & 1, abort_flag, a)) return;
+      // S_FULL: per slot; one query tile per item, per S buffer (n % 2)
+      const int s_bar = SINGLE ? (int)(n & 1u) : slot;
+      const uint32_t s_par = SINGLE ? (n >> 1) & 1u : n & 1u;
+      if (!wait_all(bar(L::S_FULL + s_bar), s_par, abort_flag, a)) return;
       RA_TR_ADD(tr, 0, tr_0);
       RA_TR_NOW(tr_1);
       tc_fence_after();
       PackedRow pk;
+      // one query tile per item: the n-th S and P in buffers n % 2; the
+      // previous PV may still be running (see mma_role_single)
+      const uint32_t tS = SINGLE ? tmem + lane_base + L::S1T_S_COL(n & 1u) : tS_pair;
+      const uint32_t tP = SINGLE ? tmem + lane_base + L::S1T_P_COL(n & 1u) : tS_pair;
+      const uint32_t pv_bar = (SINGLE && n > 0) ? bar(L::O_FREE + 0) : 0u;
+      bool tile_ok;
       if (is_diag(a, my_qt, kt))
-        softmax_tile<D, true>(tS, tP, tO, r, c, first, st, pk);
+        tile_ok = softmax_tile<D, true>(tS, tP, tO, r, c, first, st, pk, pv_bar, (n - 1) & 1,
+                                        abort_flag, a);
       else
-        softmax_tile<D, false>(tS, tP, tO, r, c, first, st, pk);
+        tile_ok = softmax_tile<D, false>(tS, tP, tO, r, c, first, st, pk, pv_bar, (n - 1) & 1,
+                                         abort_flag, a);
+      if (!tile_ok) return;
+      // One query tile per item: the previous PV may still be running (its S
+      // successor was issued two steps ahead).  Waiting for it here, before
+      // this tile's P is handed over, keeps every O_FREE wait of the slot
+      // within one phase of the barrier (the next PV cannot start before this
+      // arrive), which is what a parity wait needs; the PV is usually long done.
+      if (SINGLE && n > 0 && !wait_all(bar(L::O_FREE + 0), (n - 1) & 1, abort_flag, a)) return;
       tc_fence_before();
       __syncwarp();
-      mbar_arrive_e(bar(L::P_FULL + slot));
+      mbar_arrive_e(bar(L::P_FULL + (SINGLE ? (int)(n & 1u) : slot)));
       RA_TR_ADD(tr, 1, tr_1);
       RA_TR_NOW(tr_2);
       // the sum of the rounded weights is needed only by the epilogue: taken
@@ -1155,7 +1277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((threadIdx.x & 31) == 0) tma_role<D>(&tm_q, &tm_k, &tm_v, a, sbase, abort_flag);
     } else if (warp == kWarpMma) {
       {
-        if (a.mma_order == MMA_ORDER_GROUPED)
+        if constexpr (SINGLE)
+          mma_role_single<D>(a, sbase, tmem, abort_flag);
+        else if (a.mma_order == MMA_ORDER_GROUPED)
           mma_role<D, MMA_ORDER_GROUPED, SINGLE>(a, sbase, tmem, abort_flag);
         else if (a.mma_order == MMA_ORDER_INORDER)
           mma_role<D, MMA_ORDER_INORDER, SINGLE>(a, sbase, tmem, abort_flag);
