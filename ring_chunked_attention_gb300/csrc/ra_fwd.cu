@@ -73,8 +73,8 @@ constexpr int kThreads = 384;
 // setmaxnreg split: ptxas allocates each role's code within its share, so the
 // split decides the spills (200 / 104 left a few in the softmax code; 208 / 88
 // leaves none in the paired kernels and was 0.5-0.9 % faster, bit-identical)
-// The D = 64 kernel for single-tile items keeps 200 / 104: its MMA role spills
-// with fewer than about 104 (800 bytes of reloads at 88, 128 at 104).
+// The D = 64 kernel for single-tile items keeps 200 / 104 (ptxas: 8 bytes of
+// spill stores, 368 of spill loads; 208 / 88 the same, 192 / 120 28 and 68).
 constexpr uint32_t kLaunchRegs = 168, kSoftmaxRegs = 208, kProducerRegs = 88;
 constexpr uint32_t kSoftmaxRegs64Single = 200, kProducerRegs64Single = 104;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kProducerRegs == kThreads * kLaunchRegs,
@@ -444,13 +444,11 @@ __device__ void tma_role(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 // the previous item (bridging it as well was slower: 18.6 against 18.1 ms at
 // D = 64).
 // A launch with one query tile per item (MODE_SINGLE) leaves slot 1 idle, so
-// the kernel is built a second time (SINGLE = true) with slot 0's P stored in
-// slot 1's S columns.  S_0(u+1) then rewrites nothing that PV_0(u) reads and
-// is issued without the wait, under every order.  The softmax writes P_0(u+1)
-// over P_0(u) only after the S_FULL commit of S_0(u+1), which arrives once
-// every earlier MMA of the thread, PV_0(u) included, has completed.  Measured
-// on the S = 4096 workload (256 single-tile items): 0.0642 against 0.0667 ms,
-// bit-identical; the paired kernels are unchanged.
+// the kernel is built a second time (SINGLE = true) with a loop of its own
+// (mma_role_single) that runs S two steps ahead in slot 1's free columns; the
+// MMA order does not apply there.  S = 4096 workload (256 single-tile items):
+// 0.0457 against 0.0534 ms for the form with one S buffer, bit-identical; the
+// paired kernels are unchanged.
 // The whole MMA warp runs the loop: every wait is taken by all 32 lanes
 // (a vote makes its outcome warp-uniform), and each tcgen05.mma and
 // tcgen05.commit is issued by the one lane elect.sync picks.  Measured against
@@ -510,7 +508,10 @@ __device__ void mma_role_single(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   uint32_t q_cnt = 0;
   uint32_t c = 0;      // ring position of the current step
   bool ok = true;
+  RA_TR_DECL(tr, 10);  // the same counter slots as the paired loop's
+  RA_TR_NOW(tr_begin);
   while (ok) {
+    RA_TR_NOW(tr_item);
     if (!wait_all(bar(L::Q_FULL + 0), q_cnt & 1, abort_flag, a)) break;
     ++q_cnt;
     const int x = ld_shared_i32(sbase + L::QID_OFF);
@@ -523,12 +524,16 @@ __device__ void mma_role_single(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     // S of the step cs points at, from K at ring position cpos
     auto issue_next_s = [&](uint32_t cpos) -> bool {
       const int st = cpos % L::NS;
+      RA_TR_NOW(tr_k);
       if (!wait_all(bar(L::K_FULL + st), (cpos / L::NS) & 1, abort_flag, a)) return false;
+      RA_TR_ADD(tr, 6, tr_k);
       if (cs.kt <= lim0) {
+        RA_TR_NOW(tr_s);
         const uint32_t buf = s_cnt & 1u;
         tc_fence_after();
         issue_s<D>(tmem + L::S1T_S_COL(buf), q_lo0, k_lo0 + st * kStageLo);
         mma_commit_e(bar(L::S_FULL + (int)buf));
+        RA_TR_ADD(tr, 3, tr_s);
         ++s_cnt;
       }
       mma_commit_e(bar(L::K_EMPTY + st));
@@ -544,20 +549,32 @@ __device__ void mma_role_single(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     StepCursor cp;  // the step whose PV is issued now
     cp.init(a, it);
     bool first = true;
+    RA_TR_ADD(tr, 7, tr_item);
+    RA_TR_INC(tr, 9);
     for (int u = 0; u < ns && ok; ++u, ++c, cp.next()) {
       const int st = c % L::NS;
+      RA_TR_NOW(tr_w);
       if (!wait_all(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
+      RA_TR_ADD(tr, 2, tr_w);
+#ifdef RA_TRACE
+      if (u == 0) RA_TR_ADD(tr, 8, tr_w);
+#endif
+      RA_TR_INC(tr, 4);
       if (cp.kt <= lim0) {
         // P_FULL per P buffer: a softmax warp may run a tile ahead of the
         // others (its next S is already there), so the arrivals of tile n and
         // n + 1 go to different barriers
+        RA_TR_NOW(tr_p);
         if (!wait_all(bar(L::P_FULL + (int)(p_cnt & 1u)), (p_cnt >> 1) & 1u, abort_flag, a)) {
           ok = false;
           break;
         }
+        RA_TR_ADD(tr, 0, tr_p);
+        RA_TR_NOW(tr_i);
         tc_fence_after();
         issue_pv<D>(tO0, tmem + L::S1T_P_COL(p_cnt & 1u), v_desc(st), !first);
         mma_commit_e(bar(L::O_FREE + 0));
+        RA_TR_ADD(tr, 1, tr_i);
         ++p_cnt;
         first = false;
       }
@@ -569,20 +586,22 @@ __device__ void mma_role_single(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       }
     }
   }
+#ifdef RA_TRACE
+  RA_TR_ADD(tr, 5, tr_begin);
+  trace_store(tr, 8, 0);
+  trace_store(tr + 8, 2, 24);
+#endif
   // Every MMA this thread issued completes before tensor memory is freed.
   mma_commit_e(bar(L::DONE));
   wait_drain(bar(L::DONE), 0, a.timeout_ns);
 }
 
-template <int D, int ORDER, bool P_APART>
+template <int D, int ORDER>
 __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
                          volatile int* abort_flag) {
   using L = Layout<D>;
   auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * i; };
   const uint32_t tS0 = tmem + L::S_COL(0), tS1 = tmem + L::S_COL(1);
-  // one query tile per item: slot 0's P lives in slot 1's S columns, so the next
-  // S_0 does not rewrite it and needs no wait for the PV that reads it
-  const uint32_t tP0 = P_APART ? tS1 : tS0;
   const uint32_t tO0 = tmem + L::O_COL(0), tO1 = tmem + L::O_COL(1);
   const uint32_t q_lo0 = desc_lo(sbase + L::Q_OFF, 16);
   const uint32_t q_lo1 = desc_lo(sbase + L::Q_OFF + L::TILE, 16);
@@ -682,7 +701,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           RA_TR_ADD(tr, 0, tr_p);
           RA_TR_NOW(tr_i);
           tc_fence_after();
-          issue_pv<D>(tO0, tP0, v_desc(st), !first0);
+          issue_pv<D>(tO0, tS0, v_desc(st), !first0);
           mma_commit_e(bar(L::O_FREE + 0));
           RA_TR_ADD(tr, 1, tr_i);
           first0 = false;
@@ -701,8 +720,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         mma_commit_e(bar(L::V_EMPTY + st));
         if (m0) {
           // the PV just issued for slot 0 (the O_FREE commit of S tile s_cnt0)
-          if (!P_APART &&
-              !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+          if (!wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
           mma_commit_e(bar(L::S_FULL + 0));
@@ -725,7 +743,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           RA_TR_ADD(tr, 0, tr_p);
           RA_TR_NOW(tr_i);
           tc_fence_after();
-          issue_pv<D>(tO0, tP0, v_desc(st), !first0);
+          issue_pv<D>(tO0, tS0, v_desc(st), !first0);
           mma_commit_e(bar(L::O_FREE + 0));
           RA_TR_ADD(tr, 1, tr_i);
           first0 = false;
@@ -738,8 +756,8 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         }
         if (m0) {
           RA_TR_NOW(tr_s);
-          if (ORDER == MMA_ORDER_BRIDGED && !P_APART) tmem_shift_down_e(tS0 + 64u);
-          if (ORDER == MMA_ORDER_STRICT && !P_APART &&
+          if (ORDER == MMA_ORDER_BRIDGED) tmem_shift_down_e(tS0 + 64u);
+          if (ORDER == MMA_ORDER_STRICT &&
               !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
           tc_fence_after();
           issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
@@ -1280,13 +1298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (SINGLE)
           mma_role_single<D>(a, sbase, tmem, abort_flag);
         else if (a.mma_order == MMA_ORDER_GROUPED)
-          mma_role<D, MMA_ORDER_GROUPED, SINGLE>(a, sbase, tmem, abort_flag);
+          mma_role<D, MMA_ORDER_GROUPED>(a, sbase, tmem, abort_flag);
         else if (a.mma_order == MMA_ORDER_INORDER)
-          mma_role<D, MMA_ORDER_INORDER, SINGLE>(a, sbase, tmem, abort_flag);
+          mma_role<D, MMA_ORDER_INORDER>(a, sbase, tmem, abort_flag);
         else if (a.mma_order == MMA_ORDER_BRIDGED)
-          mma_role<D, MMA_ORDER_BRIDGED, SINGLE>(a, sbase, tmem, abort_flag);
+          mma_role<D, MMA_ORDER_BRIDGED>(a, sbase, tmem, abort_flag);
         else
-          mma_role<D, MMA_ORDER_STRICT, SINGLE>(a, sbase, tmem, abort_flag);
+          mma_role<D, MMA_ORDER_STRICT>(a, sbase, tmem, abort_flag);
       }
     }
   }

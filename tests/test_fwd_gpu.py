@@ -390,9 +390,9 @@ def test_mma_orders_are_bit_identical(ralib, cuda_ok, name):
     Any ordering hazard would corrupt P and show up as a difference.  Every
     workload runs under every order twice: with paired query tiles forced (the
     pairs are where the orders differ) and with one query tile per item forced
-    (P then sits in the idle slot's columns and the next S is issued without
-    waiting for the PV).  Pairing changes which SM runs a tile, not its
-    arithmetic, so all ten results are the same bits."""
+    (those launches run their own loop, S two steps ahead in double-buffered
+    columns, whatever the order).  Pairing changes which SM runs a tile, not
+    its arithmetic, so all ten results are the same bits."""
     w = WORKLOADS[name] if name in WORKLOADS else Workload("small", 2, 8, 2, 2048, 128, 4, True)
     q, k, v = make_inputs(w, seed=43)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
