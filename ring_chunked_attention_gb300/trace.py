@@ -4,12 +4,15 @@ Run with the traced library selected (``RA_TRACE=1``; built by
 ``python -m ring_chunked_attention_gb300.build --trace``):
 
     RA_TRACE=1 python -m ring_chunked_attention_gb300.trace --workload gqa_s16384
+    RA_TRACE=1 python -m ring_chunked_attention_gb300.trace --workload d64_s32768 --pairing 2
 
 It launches ``ra_fwd`` on the workload's seeded inputs (three launches, the
 last one counted), reads the counters with ``ra_trace_read`` and prints, per
 key/value step of one CTA (both query slots), where the MMA warp, the softmax
-warps of each slot and the producer thread spend their cycles.  The counting
-itself lengthens the launch by about a tenth; compare shapes, not absolutes.
+warps of each slot and the producer thread spend their cycles.  ``--pairing``
+forces paired query tiles (1) or one query tile per item (2), as
+``ra_set_item_pairing`` does.  The counting itself lengthens the launch by
+about a tenth; compare shapes, not absolutes.
 """
 from __future__ import annotations
 
@@ -57,6 +60,8 @@ def summarize(counters):
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--workload", default="gqa_s16384")
+    ap.add_argument("--pairing", type=int, default=0, choices=(0, 1, 2),
+                    help="0 automatic, 1 paired query tiles, 2 one query tile per item")
     args = ap.parse_args(argv)
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     if root not in sys.path:
@@ -72,13 +77,17 @@ def main(argv=None) -> int:
         return 2
     w = WORKLOADS[args.workload]
     q, k, v = (t.cuda() for t in make_inputs(w))
-    for _ in range(3):
-        ra.ra_fwd(q, k, v, P=w.P, causal=w.causal)
-    torch.cuda.synchronize()
+    ra.ra_set_item_pairing(args.pairing)
+    try:
+        for _ in range(3):
+            ra.ra_fwd(q, k, v, P=w.P, causal=w.causal)
+        torch.cuda.synchronize()
+    finally:
+        ra.ra_set_item_pairing(0)
     status = ra.ra_get_last_device_status()
     ctas = min(torch.cuda.get_device_properties(0).multi_processor_count, 1024)
     res = summarize(ra.ra_trace_read(ctas))
-    print(f"{w.name}: status {ra.ra_status_string(status)}")
+    print(f"{w.name} (pairing {args.pairing}): status {ra.ra_status_string(status)}")
     for key, val in res.items():
         print(f"  {key}: {val:,.0f}" if isinstance(val, float) else f"  {key}: {val}")
     return 0 if status == ra.RA_OK else 1
