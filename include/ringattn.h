@@ -328,8 +328,10 @@ ra_status ra_trace_read(unsigned long long* out, int n_ctas);
  *     accumulators in issue order, which no document states.  For measurement
  *     and tests only.
  * All four compute the same arithmetic; the test-suite checks that their
- * outputs are bit-identical.  Other values select order 3.  Applies to
- * launches made after the call.
+ * outputs are bit-identical.  Other values select order 3.  Launches with one
+ * query tile per item (see ra_set_item_pairing) keep S and P in separate,
+ * double-buffered columns, issue each S two steps ahead of its PV, and are
+ * not affected by the order.  Applies to launches made after the call.
  */
 void ra_set_mma_order(int order);
 
@@ -340,8 +342,10 @@ void ra_set_mma_order(int order);
  * heads of a GQA group, or two consecutive tiles of one head); a single item
  * is one tile.  policy 0 (default): pair, unless that leaves fewer items than
  * the device has SMs, when single items shorten the heaviest item; 1: pair
- * whenever the shape allows; 2: never pair.  Results agree to rounding; the
- * policy exists so that tests can reach every grouping at small sizes.
+ * whenever the shape allows; 2: never pair.  The grouping changes which SM
+ * computes a tile, not its arithmetic: results are the same bits under every
+ * policy.  The policy exists so that tests can reach every grouping at small
+ * sizes.
  * Applies to launches made after the call.
  */
 void ra_set_item_pairing(int policy);
