@@ -175,12 +175,15 @@ def test_lse_optional(ralib, cuda_ok):
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("sigma", [3.0, 6.0])
-def test_peaked_softmax_rescaling(ralib, cuda_ok, oracle_mod, D, sigma):
+def test_peaked_softmax_rescaling(ralib, cuda_ok, oracle_mod, D, sigma, pairing):
     """std sigma on q and k: scores with std sigma^2 (x sqrt(D) scale), so a
     row's max jumps by far more than the 2^8 rescale threshold between tiles;
     at sigma = 6 the jumps also pass the 2^30 guard of the skipped max pass,
     so warps take the exact path (max pass, O rescale, which at D = 64 also
-    rescales the PV MMA's row-sum columns)."""
+    rescales the PV MMA's row-sum columns).  At this size automatic grouping
+    gives one query tile per item (where the O rescale first waits for the
+    previous PV, which runs behind the next S); forced pairing runs the
+    two-tile kernel's exact path."""
     w = Workload("peak", 1, 2, 2, 1024, D, 4, True, sigma_qk=sigma)
     q, k, v = make_inputs(w, seed=23)
     out, lse = _run(ralib, q, k, v, w)
@@ -189,14 +192,15 @@ def test_peaked_softmax_rescaling(ralib, cuda_ok, oracle_mod, D, sigma):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-def test_late_dominant_key_takes_the_exact_path(ralib, cuda_ok, oracle_mod, D):
+def test_late_dominant_key_takes_the_exact_path(ralib, cuda_ok, oracle_mod, D, pairing):
     """One key of chunk 0 scores about 50 (natural units, 72 in log2 units)
     above everything else for every row of chunks 1-3.  Those rows visit
     chunk 0 last in ring order, so by then their reference max is far below
     it: the speculative exps exceed the 2^30 guard and every such warp must
     take the exact path (scores streamed back from tensor memory, new
     reference, O rescaled by about 2^-72).  The output is then dominated by
-    that key's value row."""
+    that key's value row.  Run with one query tile per item (automatic at
+    this size) and with paired items."""
     w = Workload("late", 1, 2, 1, 1024, D, 4, True)
     q, k, v = make_inputs(w, seed=31)
     t = 5                                   # the planted key (chunk 0, first tile)
