@@ -618,12 +618,13 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   uint32_t q_cnt0 = 0, q_cnt1 = 0;
   uint32_t c = 0;                   // ring position of the current step
   bool ok = true;
-  RA_TR_DECL(tr, 10);
+  RA_TR_DECL(tr, 12);
   RA_TR_NOW(tr_begin);
 
   while (ok) {
     RA_TR_NOW(tr_item);
     // the next item with work: its id comes with its first query tile (-1: none left)
+    RA_TR_NOW(tr_q);
     if (!wait_all(bar(L::Q_FULL + 0), q_cnt0 & 1, abort_flag, a)) break;
     ++q_cnt0;
     const int x = ld_shared_i32(sbase + L::QID_OFF);
@@ -634,6 +635,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       if (!wait_all(bar(L::Q_FULL + 1), q_cnt1 & 1, abort_flag, a)) break;
       ++q_cnt1;
     }
+    RA_TR_ADD(tr, 10, tr_q);
     // slot i needs key tile kt iff kt <= lim_i (needs_tile's causal test,
     // taken once per item instead of per step; -1: the item has no slot 1)
     const int lim0 = a.causal ? a.q_tile0 + it.qt[0] - a.k_tile0 : INT_MAX;
@@ -645,14 +647,18 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
       const int st = c % L::NS;
       if (!wait_all(bar(L::K_FULL + st), (c / L::NS) & 1, abort_flag, a)) break;
       if (nxt.kt <= lim0) {
+        RA_TR_NOW(tr_o);
         if (s_cnt0 > 0 && !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) break;
+        RA_TR_ADD(tr, 11, tr_o);
         tc_fence_after();
         issue_s<D>(tS0, q_lo0, k_lo0 + st * kStageLo);
         mma_commit_e(bar(L::S_FULL + 0));
         ++s_cnt0;
       }
       if (nxt.kt <= lim1) {
+        RA_TR_NOW(tr_o);
         if (s_cnt1 > 0 && !wait_all(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) break;
+        RA_TR_ADD(tr, 11, tr_o);
         tc_fence_after();
         issue_s<D>(tS1, q_lo1, k_lo0 + st * kStageLo);
         mma_commit_e(bar(L::S_FULL + 1));
@@ -801,6 +807,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   RA_TR_ADD(tr, 5, tr_begin);
   trace_store(tr, 8, 0);
   trace_store(tr + 8, 2, 24);
+  trace_store(tr + 10, 2, 26);
 #endif
   // Every MMA this thread issued completes before tensor memory is freed.
   mma_commit_e(bar(L::DONE));

@@ -110,8 +110,9 @@ __device__ __forceinline__ bool in_bounds(size_t first, size_t count, size_t ext
 // 4 steps, 5 role total, 6 late K waits, 7 item starts (Q waits and the first
 // S); softmax slot 0 warp 0 at 8.., slot 1 (warp 4) at 16..: +0 S waits,
 // +1 S to P hand-off, +2 after the hand-off, +3 tiles, +4 epilogues, +5 items;
-// 24 V waits at an item's first step, 25 items (MMA warp); producer 28 K-stage
-// waits, 29 V-stage waits, 30 Q-slot waits.
+// 24 V waits at an item's first step, 25 items, 26 Q waits and 27 waits for
+// the previous item's last PV inside the item starts (MMA warp, paired items);
+// producer 28 K-stage waits, 29 V-stage waits, 30 Q-slot waits.
 constexpr int kTraceSlots = 32;
 constexpr int kTraceCtas = 1024;
 #ifdef RA_TRACE

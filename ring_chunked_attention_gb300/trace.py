@@ -24,6 +24,7 @@ import sys
 MMA = {"P waits": 0, "PV issue": 1, "V waits": 2, "S issue": 3, "late K waits": 6,
        "item starts": 7}
 MMA_STEPS, MMA_TOTAL, MMA_FIRST_V, MMA_ITEMS = 4, 5, 24, 25
+MMA_ITEM = {"Q waits": 26, "waits for the previous item's last PV": 27}
 SOFTMAX = {"S waits": 0, "S to P hand-off": 1, "after the hand-off": 2}
 SOFTMAX_TILES, SOFTMAX_EPI, SOFTMAX_ITEMS = 3, 4, 5
 PRODUCER = {"K-stage waits": 28, "V-stage waits": 29}
@@ -54,6 +55,8 @@ def summarize(counters):
     if items:
         out["producer: Q-slot waits per item"] = float(c[:, PRODUCER_Q].sum()) / items
         out["MMA warp: V waits at an item's first step, per item"] = float(c[:, MMA_FIRST_V].sum()) / items
+        for name, i in MMA_ITEM.items():
+            out[f"MMA warp: item start, {name}, per item"] = float(c[:, i].sum()) / items
     return out
 
 
