@@ -618,7 +618,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   uint32_t q_cnt0 = 0, q_cnt1 = 0;
   uint32_t c = 0;                   // ring position of the current step
   bool ok = true;
-  RA_TR_DECL(tr, 12);
+  RA_TR_DECL(tr, 14);
   RA_TR_NOW(tr_begin);
 
   while (ok) {
@@ -674,12 +674,14 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
     RA_TR_ADD(tr, 7, tr_item);
     RA_TR_INC(tr, 9);
     for (int u = 0; u < ns && ok; ++u, ++c) {
+      RA_TR_NOW(tr_top);
       const int st = c % L::NS;
       const bool n0 = nxt.kt <= lim0, n1 = nxt.kt <= lim1;
       const bool more = u + 1 < ns;
       if (more) nxt.next();
       const bool m0 = more && nxt.kt <= lim0, m1 = more && nxt.kt <= lim1;
       const int st1 = (c + 1) % L::NS;
+      RA_TR_ADD(tr, 12, tr_top);
       RA_TR_NOW(tr_w);
       if (!wait_all(bar(L::V_FULL + st), (c / L::NS) & 1, abort_flag, a)) { ok = false; break; }
       RA_TR_ADD(tr, 2, tr_w);
@@ -794,8 +796,10 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           RA_TR_ADD(tr, 3, tr_s);
           ++s_cnt1;
         }
+        RA_TR_NOW(tr_end);
         mma_commit_e(bar(L::V_EMPTY + st));
         if (more) mma_commit_e(bar(L::K_EMPTY + st1));
+        RA_TR_ADD(tr, 13, tr_end);
       }
       if (u + 2 == ns) {  // the item's last S MMAs are issued: its Q tiles may be replaced
         mma_commit_e(bar(L::Q_EMPTY + 0));
@@ -808,6 +812,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
   trace_store(tr, 8, 0);
   trace_store(tr + 8, 2, 24);
   trace_store(tr + 10, 2, 26);
+  trace_store(tr + 12, 2, 14);
 #endif
   // Every MMA this thread issued completes before tensor memory is freed.
   mma_commit_e(bar(L::DONE));

@@ -111,7 +111,8 @@ __device__ __forceinline__ bool in_bounds(size_t first, size_t count, size_t ext
 // S); softmax slot 0 warp 0 at 8.., slot 1 (warp 4) at 16..: +0 S waits,
 // +1 S to P hand-off, +2 after the hand-off, +3 tiles, +4 epilogues, +5 items;
 // 24 V waits at an item's first step, 25 items, 26 Q waits and 27 waits for
-// the previous item's last PV inside the item starts (MMA warp, paired items);
+// the previous item's last PV inside the item starts, 14 each step's top (up
+// to its V wait) and 15 its closing commits (MMA warp, paired items);
 // producer 28 K-stage waits, 29 V-stage waits, 30 Q-slot waits.
 constexpr int kTraceSlots = 32;
 constexpr int kTraceCtas = 1024;

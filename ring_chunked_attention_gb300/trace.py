@@ -22,7 +22,7 @@ import sys
 
 # counter slots per CTA (see ra_internal.h)
 MMA = {"P waits": 0, "PV issue": 1, "V waits": 2, "S issue": 3, "late K waits": 6,
-       "item starts": 7}
+       "item starts": 7, "step top": 14, "closing commits": 15}
 MMA_STEPS, MMA_TOTAL, MMA_FIRST_V, MMA_ITEMS = 4, 5, 24, 25
 MMA_ITEM = {"Q waits": 26, "waits for the previous item's last PV": 27}
 SOFTMAX = {"S waits": 0, "S to P hand-off": 1, "after the hand-off": 2}
