@@ -34,9 +34,13 @@ constexpr uint32_t kDescHiSw128 = ((1024u >> 4) & 0x3FFFu) | (1u << 14) | (2u <<
 // abort flag.
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned long long timeout_ns, unsigned int* status) {
-  const uint64_t t0 = global_timer_ns();
+  // the timeout's reference is read only once a first sleeping wait has
+  // returned without the phase: most waits end there, and the timer read
+  // would lie on their path
+  uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    if (it == 1) t0 = global_timer_ns();
     if ((it & 3u) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > timeout_ns) {
