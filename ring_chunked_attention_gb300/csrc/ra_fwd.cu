@@ -868,25 +868,39 @@ struct PackedRow {  // a row's 128 bf16 weights in pairs, by 32-column chunk
   uint32_t a[16], b[16], c[16], d[16];
 };
 
-__device__ __forceinline__ void rounded_sum_chunk(const uint32_t (&pk)[16], uint64_t& s0,
-                                                  uint64_t& s1) {
+// s_lo += low bf16 of p, s_hi += high bf16 of p (fp32 sums, round to nearest)
+__device__ __forceinline__ void add_bf16_halves(uint32_t p, float& s_lo, float& s_hi) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(s_lo), "+f"(s_hi)
+      : "r"(p));
+}
+
+// Four running sums: even pairs' low and high halves, odd pairs' low and high
+// halves, each a chain of fp32 additions in pair order
+struct RoundedSums {
+  float e_lo, e_hi, o_lo, o_hi;
+};
+
+__device__ __forceinline__ void rounded_sum_chunk(const uint32_t (&pk)[16], RoundedSums& s) {
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
-    s0 = f2_add(s0, ((uint64_t)(pk[i] & 0xFFFF0000u) << 32) | (uint64_t)(pk[i] << 16));
-    s1 = f2_add(s1, ((uint64_t)(pk[i + 1] & 0xFFFF0000u) << 32) | (uint64_t)(pk[i + 1] << 16));
+    add_bf16_halves(pk[i], s.e_lo, s.e_hi);
+    add_bf16_halves(pk[i + 1], s.o_lo, s.o_hi);
   }
 }
 
 // fp32 sum of the row's bf16 weights: the normaliser of the output, which
 // accumulates exactly these rounded values
 __device__ __forceinline__ float rounded_sum(const PackedRow& pk) {
-  uint64_t s0 = 0, s1 = 0;
-  rounded_sum_chunk(pk.a, s0, s1);
-  rounded_sum_chunk(pk.b, s0, s1);
-  rounded_sum_chunk(pk.c, s0, s1);
-  rounded_sum_chunk(pk.d, s0, s1);
-  const uint64_t t = f2_add(s0, s1);
-  return f2_lo(t) + f2_hi(t);
+  RoundedSums s{0.0f, 0.0f, 0.0f, 0.0f};
+  rounded_sum_chunk(pk.a, s);
+  rounded_sum_chunk(pk.b, s);
+  rounded_sum_chunk(pk.c, s);
+  rounded_sum_chunk(pk.d, s);
+  return (s.e_lo + s.o_lo) + (s.e_hi + s.o_hi);
 }
 
 struct RowState {
