@@ -982,14 +982,8 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tP, uint32_t 
   float se;
   {
     uint32_t va[32], vb[32], vc[32], vd[32];
-    tmem_ld32(tS + 0, va);
-    tmem_ld32(tS + 32, vb);
-    tmem_ld32(tS + 64, vc);
-    tmem_ld32(tS + 96, vd);
-    tmem_wait_ld_regs(va);
-    tmem_wait_ld_regs(vb);
-    tmem_wait_ld_regs(vc);
-    tmem_wait_ld_regs(vd);
+    tmem_ld128(tS, va, vb, vc, vd);
+    tmem_wait_ld128(va, vb, vc, vd);
     if (first) st.m = row_max<DIAG>(va, vb, vc, vd, r) * c;
     se = exp_row<DIAG>(va, vb, vc, vd, r, c, st.m, pk);
   }
@@ -1047,10 +1041,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tP, uint32_t 
     const uint64_t sum = f2_add(se0, se1);
     se = f2_lo(sum) + f2_hi(sum);
   }
-  tmem_st16(tP + 0, pk.a);
-  tmem_st16(tP + 16, pk.b);
-  tmem_st16(tP + 32, pk.c);
-  tmem_st16(tP + 48, pk.d);
+  tmem_st64(tP, pk.a, pk.b, pk.c, pk.d);
   st.l_exact += se;
   tmem_wait_st();
   return true;
