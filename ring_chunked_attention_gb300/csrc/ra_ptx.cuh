@@ -203,6 +203,79 @@ __device__ __forceinline__ void mma_ts_lh_e(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Groups of N MMAs into one accumulator, issued under a single elect.sync:
+// the first accumulates into D when first_acc is non-zero, the others always.
+// SS: A and B from shared-memory descriptors (low words a[k], b[k], common
+// high word hi); TS: A from tensor memory at a[k], B from a descriptor.
+template <int N>
+__device__ __forceinline__ void mma_ss_group_e(uint32_t d_tmem, const uint32_t (&a)[N],
+                                               const uint32_t (&b)[N], uint32_t hi, uint32_t idesc,
+                                               uint32_t first_acc);
+template <int N>
+__device__ __forceinline__ void mma_ts_group_e(uint32_t d_tmem, const uint32_t (&a)[N],
+                                               const uint32_t (&b)[N], uint32_t hi, uint32_t idesc,
+                                               uint32_t first_acc);
+template <>
+__device__ __forceinline__ void mma_ss_group_e<4>(uint32_t d_tmem, const uint32_t (&a)[4],
+                                                   const uint32_t (&b)[4], uint32_t hi,
+                                                   uint32_t idesc, uint32_t first_acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 db;\n\t"
+      ".reg .b64 da;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %3, 0;\n\t"
+      "setp.eq.b32 t, %1, %1;\n\t"
+      "mov.b64 da, {%4, %1};\n\t"
+      "mov.b64 db, {%8, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %2, p;\n\t"
+      "mov.b64 da, {%5, %1};\n\t"
+      "mov.b64 db, {%9, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %2, t;\n\t"
+      "mov.b64 da, {%6, %1};\n\t"
+      "mov.b64 db, {%10, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %2, t;\n\t"
+      "mov.b64 da, {%7, %1};\n\t"
+      "mov.b64 db, {%11, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %2, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(hi), "r"(idesc), "r"(first_acc), "r"(a[0]), "r"(a[1]),
+        "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3])
+      : "memory");
+}
+
+template <>
+__device__ __forceinline__ void mma_ts_group_e<8>(uint32_t d_tmem, const uint32_t (&a)[8],
+                                                   const uint32_t (&b)[8], uint32_t hi,
+                                                   uint32_t idesc, uint32_t first_acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 db;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %3, 0;\n\t"
+      "setp.eq.b32 t, %1, %1;\n\t"
+      "mov.b64 db, {%12, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], db, %2, p;\n\t"
+      "mov.b64 db, {%13, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], db, %2, t;\n\t"
+      "mov.b64 db, {%14, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], db, %2, t;\n\t"
+      "mov.b64 db, {%15, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], db, %2, t;\n\t"
+      "mov.b64 db, {%16, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], db, %2, t;\n\t"
+      "mov.b64 db, {%17, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], db, %2, t;\n\t"
+      "mov.b64 db, {%18, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], db, %2, t;\n\t"
+      "mov.b64 db, {%19, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], db, %2, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(hi), "r"(idesc), "r"(first_acc), "r"(a[0]), "r"(a[1]),
+        "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+        "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]),
+        "r"(b[6]), "r"(b[7])
+      : "memory");
+}
+
 // one arrive on an mbarrier for the whole warp, from the lane elect.sync picks
 // (a predicated instruction: no divergent branch)
 __device__ __forceinline__ void mbar_arrive_e(uint32_t bar) {
