@@ -504,6 +504,52 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo
   }
 }
 
+// A PV product and the commit of its completion to `bar`; at D = 64 under one
+// elect.sync (the same instructions in the same order)
+template <int D>
+__device__ __forceinline__ void issue_pv_commit(uint32_t tO, uint32_t tP, uint32_t v_lo,
+                                                bool accumulate, uint32_t bar) {
+  if constexpr (D == 64) {
+    constexpr uint32_t idesc_pv = make_idesc(kBM, Layout<D>::OW, 1);
+    uint32_t pa[kBN / 16], vb[kBN / 16];
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+      pa[kk] = tP + kk * 8;
+      vb[kk] = v_lo + (uint32_t)(kk * (2048 >> 4));
+    }
+    mma_ts_group8_commit_e(tO, pa, vb, kDescHiSw128, idesc_pv, accumulate ? 1u : 0u, bar);
+  } else {
+    issue_pv<D>(tO, tP, v_lo, accumulate);
+    mma_commit_e(bar);
+  }
+}
+
+// The bridged order's next S: a tcgen05.shift of 8 consumed S columns, the S
+// product and the commit of its completion to `bar`; at D = 64 under one
+// elect.sync, after the fence (the same instructions in the same order)
+template <int D>
+__device__ __forceinline__ void issue_shift_s_commit(uint32_t shift_taddr, uint32_t tS,
+                                                     uint32_t q_lo, uint32_t k_lo, uint32_t bar) {
+  if constexpr (D == 64) {
+    using L = Layout<D>;
+    constexpr uint32_t idesc_s = make_idesc(kBM, kBN, 0);
+    uint32_t qa[D / 16], kb[D / 16];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (uint32_t)((kk >> 2) * L::BLOCK + (kk & 3) * 32) >> 4;
+      qa[kk] = q_lo + off;
+      kb[kk] = k_lo + off;
+    }
+    tc_fence_after();
+    mma_shift_ss_group4_commit_e(shift_taddr, tS, qa, kb, kDescHiSw128, idesc_s, bar);
+  } else {
+    tmem_shift_down_e(shift_taddr);
+    tc_fence_after();
+    issue_s<D>(tS, q_lo, k_lo);
+    mma_commit_e(bar);
+  }
+}
+
 // One query tile per item (slot 1 idle): S runs two steps ahead of PV.  The
 // n-th S goes to buffer n % 2 and the softmax writes the n-th P to P buffer
 // n % 2, so S(u+2) can start as soon as the softmax has handed over P(u), and
@@ -775,8 +821,7 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           RA_TR_ADD(tr, 0, tr_p);
           RA_TR_NOW(tr_i);
           tc_fence_after();
-          issue_pv<D>(tO0, tS0, v_desc(st), !first0);
-          mma_commit_e(bar(L::O_FREE + 0));
+          issue_pv_commit<D>(tO0, tS0, v_desc(st), !first0, bar(L::O_FREE + 0));
           RA_TR_ADD(tr, 1, tr_i);
           first0 = false;
         }
@@ -788,12 +833,15 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
         }
         if (m0) {
           RA_TR_NOW(tr_s);
-          if (ORDER == MMA_ORDER_BRIDGED) tmem_shift_down_e(tS0 + 64u);
-          if (ORDER == MMA_ORDER_STRICT &&
-              !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
-          tc_fence_after();
-          issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
-          mma_commit_e(bar(L::S_FULL + 0));
+          if constexpr (ORDER == MMA_ORDER_BRIDGED) {
+            issue_shift_s_commit<D>(tS0 + 64u, tS0, q_lo0, k_lo0 + st1 * kStageLo, bar(L::S_FULL + 0));
+          } else {
+            if (ORDER == MMA_ORDER_STRICT &&
+                !wait_all(bar(L::O_FREE + 0), (s_cnt0 - 1) & 1, abort_flag, a)) { ok = false; break; }
+            tc_fence_after();
+            issue_s<D>(tS0, q_lo0, k_lo0 + st1 * kStageLo);
+            mma_commit_e(bar(L::S_FULL + 0));
+          }
           RA_TR_ADD(tr, 3, tr_s);
           ++s_cnt0;
         }
@@ -804,25 +852,31 @@ __device__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t tmem,
           RA_TR_ADD(tr, 0, tr_p);
           RA_TR_NOW(tr_i);
           tc_fence_after();
-          issue_pv<D>(tO1, tS1, v_desc(st), !first1);
-          mma_commit_e(bar(L::O_FREE + 1));
+          issue_pv_commit<D>(tO1, tS1, v_desc(st), !first1, bar(L::O_FREE + 1));
           RA_TR_ADD(tr, 1, tr_i);
           first1 = false;
         }
         if (m1) {
           RA_TR_NOW(tr_s);
-          if (ORDER == MMA_ORDER_BRIDGED) tmem_shift_down_e(tS1 + 64u);
-          if (ORDER == MMA_ORDER_STRICT && s_cnt1 > 0 &&
-              !wait_all(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
-          tc_fence_after();
-          issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);
-          mma_commit_e(bar(L::S_FULL + 1));
+          if constexpr (ORDER == MMA_ORDER_BRIDGED) {
+            issue_shift_s_commit<D>(tS1 + 64u, tS1, q_lo1, k_lo0 + st1 * kStageLo, bar(L::S_FULL + 1));
+          } else {
+            if (ORDER == MMA_ORDER_STRICT && s_cnt1 > 0 &&
+                !wait_all(bar(L::O_FREE + 1), (s_cnt1 - 1) & 1, abort_flag, a)) { ok = false; break; }
+            tc_fence_after();
+            issue_s<D>(tS1, q_lo1, k_lo0 + st1 * kStageLo);
+            mma_commit_e(bar(L::S_FULL + 1));
+          }
           RA_TR_ADD(tr, 3, tr_s);
           ++s_cnt1;
         }
         RA_TR_NOW(tr_end);
-        mma_commit_e(bar(L::V_EMPTY + st));
-        if (more) mma_commit_e(bar(L::K_EMPTY + st1));
+        if constexpr (D == 64) {
+          mma_commit2_e(bar(L::V_EMPTY + st), bar(L::K_EMPTY + st1), more ? 1u : 0u);
+        } else {
+          mma_commit_e(bar(L::V_EMPTY + st));
+          if (more) mma_commit_e(bar(L::K_EMPTY + st1));
+        }
         RA_TR_ADD(tr, 13, tr_end);
       }
       if (u + 2 == ns) {  // the item's last S MMAs are issued: its Q tiles may be replaced

@@ -276,6 +276,87 @@ __device__ __forceinline__ void mma_ts_group_e<8>(uint32_t d_tmem, const uint32_
       : "memory");
 }
 
+// A PV group of 8 MMAs and the commit of its completion to `bar`, under one
+// elect.sync (the MMAs as in mma_ts_group_e)
+__device__ __forceinline__ void mma_ts_group8_commit_e(uint32_t d_tmem, const uint32_t (&a)[8],
+                                                       const uint32_t (&b)[8], uint32_t hi,
+                                                       uint32_t idesc, uint32_t first_acc,
+                                                       uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 db;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %3, 0;\n\t"
+      "setp.eq.b32 t, %1, %1;\n\t"
+      "mov.b64 db, {%13, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], db, %2, p;\n\t"
+      "mov.b64 db, {%14, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], db, %2, t;\n\t"
+      "mov.b64 db, {%15, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], db, %2, t;\n\t"
+      "mov.b64 db, {%16, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], db, %2, t;\n\t"
+      "mov.b64 db, {%17, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], db, %2, t;\n\t"
+      "mov.b64 db, {%18, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], db, %2, t;\n\t"
+      "mov.b64 db, {%19, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], db, %2, t;\n\t"
+      "mov.b64 db, {%20, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%12], db, %2, t;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}"
+      ::"r"(d_tmem), "r"(hi), "r"(idesc), "r"(first_acc), "r"(bar), "r"(a[0]),
+        "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]),
+        "r"(a[7]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]),
+        "r"(b[5]), "r"(b[6]), "r"(b[7])
+      : "memory");
+}
+
+// A tcgen05.shift.down of the 32-byte column block at shift_taddr, an S
+// group of 4 MMAs (the first overwriting D) and the commit of their
+// completion to `bar`, under one elect.sync: shift -> MMA execute in issue
+// order, as with separate instructions
+__device__ __forceinline__ void mma_shift_ss_group4_commit_e(uint32_t shift_taddr, uint32_t d_tmem,
+                                                             const uint32_t (&a)[4],
+                                                             const uint32_t (&b)[4], uint32_t hi,
+                                                             uint32_t idesc, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, f, t;\n\t.reg .b64 da, db;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %1, %1;\n\t"
+      "setp.eq.b32 t, %1, %1;\n\t"
+      "@e tcgen05.shift.cta_group::1.down [%5];\n\t"
+      "mov.b64 da, {%6, %1};\n\t"
+      "mov.b64 db, {%10, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %2, f;\n\t"
+      "mov.b64 da, {%7, %1};\n\t"
+      "mov.b64 db, {%11, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %2, t;\n\t"
+      "mov.b64 da, {%8, %1};\n\t"
+      "mov.b64 db, {%12, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %2, t;\n\t"
+      "mov.b64 da, {%9, %1};\n\t"
+      "mov.b64 db, {%13, %1};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %2, t;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%3];\n\t}"
+      ::"r"(d_tmem), "r"(hi), "r"(idesc), "r"(bar), "r"(0u), "r"(shift_taddr),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]),
+        "r"(b[2]), "r"(b[3])
+      : "memory");
+}
+
+// Commits to bar0 and, when has1 is non-zero, to bar1, under one elect.sync
+__device__ __forceinline__ void mma_commit2_e(uint32_t bar0, uint32_t bar1, uint32_t has1) {
+  asm volatile(
+      "{\n\t.reg .pred e, h, q;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 h, %2, 0;\n\t"
+      "and.pred q, e, h;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}"
+      ::"r"(bar0), "r"(bar1), "r"(has1)
+      : "memory");
+}
+
 // one arrive on an mbarrier for the whole warp, from the lane elect.sync picks
 // (a predicated instruction: no divergent branch)
 __device__ __forceinline__ void mbar_arrive_e(uint32_t bar) {
