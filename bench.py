@@ -413,14 +413,16 @@ def ceilings_obj(ra, tensor_peak: float):
     return out
 
 
-def measure_e2e(ra, w, q, k, v, flush, steps: int):
+def measure_e2e(ra, w, q, k, v, flush, steps: int, warmup: int = 3):
     """End to end through ra_fwd with the inputs in pinned host memory: every
     step copies its q, k, v host -> device, runs the forward and reads out and
     lse back device -> host.  Steps are pipelined over two device buffer sets
     and three streams (copy in, compute, copy out), with events for every
     dependency: step i's inputs upload while step i-1 computes and step i-2's
-    results download.  Returns (ms per step over the whole run, host->device
-    bytes per step, device->host bytes per step, steps)."""
+    results download.  The same pipeline first runs `warmup` untimed steps
+    (the first copies from freshly pinned buffers and the first work on new
+    streams), then `steps` timed ones.  Returns (ms per step over the timed
+    run, host->device bytes per step, device->host bytes per step, steps)."""
     import torch
 
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
@@ -434,35 +436,43 @@ def measure_e2e(ra, w, q, k, v, flush, steps: int):
     h2d = (qh.numel() + kh.numel() + vh.numel()) * 2
     d2h = outh[0].numel() * 2 + lseh[0].numel() * 4
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(steps)]
-    ev_comp = [torch.cuda.Event() for _ in range(steps)]
-    ev_out = [torch.cuda.Event() for _ in range(steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def pipeline(n, t0=None, t1=None):
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_comp = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        if t0 is not None:
+            t0.record(s_in)
+        for i in range(n):
+            bq, bk, bv, bo, bl = dev[i % 2]
+            if i >= 2:
+                s_in.wait_event(ev_comp[i - 2])  # the kernel of step i-2 is done with these inputs
+            with torch.cuda.stream(s_in):
+                bq.copy_(qh, non_blocking=True)
+                bk.copy_(kh, non_blocking=True)
+                bv.copy_(vh, non_blocking=True)
+            ev_in[i].record(s_in)
+            s_comp.wait_event(ev_in[i])
+            if i >= 2:
+                s_comp.wait_event(ev_out[i - 2])  # step i-2's results were read back
+            with torch.cuda.stream(s_comp):
+                flush.fill_(1.0)
+                ra.ra_fwd(bq, bk, bv, P=w.P, causal=w.causal, scale=w.scale, out=bo, lse=bl,
+                          stream=s_comp)
+            ev_comp[i].record(s_comp)
+            s_out.wait_event(ev_comp[i])
+            with torch.cuda.stream(s_out):
+                outh[i % 2].copy_(bo, non_blocking=True)
+                lseh[i % 2].copy_(bl, non_blocking=True)
+            ev_out[i].record(s_out)
+        if t1 is not None:
+            t1.record(s_out)
+
     torch.cuda.synchronize()
-    t0.record(s_in)
-    for i in range(steps):
-        bq, bk, bv, bo, bl = dev[i % 2]
-        if i >= 2:
-            s_in.wait_event(ev_comp[i - 2])  # the kernel of step i-2 is done with these inputs
-        with torch.cuda.stream(s_in):
-            bq.copy_(qh, non_blocking=True)
-            bk.copy_(kh, non_blocking=True)
-            bv.copy_(vh, non_blocking=True)
-        ev_in[i].record(s_in)
-        s_comp.wait_event(ev_in[i])
-        if i >= 2:
-            s_comp.wait_event(ev_out[i - 2])  # step i-2's results were read back
-        with torch.cuda.stream(s_comp):
-            flush.fill_(1.0)
-            ra.ra_fwd(bq, bk, bv, P=w.P, causal=w.causal, scale=w.scale, out=bo, lse=bl,
-                      stream=s_comp)
-        ev_comp[i].record(s_comp)
-        s_out.wait_event(ev_comp[i])
-        with torch.cuda.stream(s_out):
-            outh[i % 2].copy_(bo, non_blocking=True)
-            lseh[i % 2].copy_(bl, non_blocking=True)
-        ev_out[i].record(s_out)
-    t1.record(s_out)
+    pipeline(warmup)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pipeline(steps, t0, t1)
     torch.cuda.synchronize()
     if ra.ra_get_last_device_status() != 0:
         raise RuntimeError("device status reported a timeout in the end-to-end steps")
@@ -534,7 +544,8 @@ def run_ours(args):
     ms = statistics.mean(kernel_ms)
 
     # end to end through the public call with host buffers (pinned), copies timed
-    e2e_ms, h2d, d2h, e2e_steps = measure_e2e(ra, w, q, k, v, flush, max(10, min(args.steps, 30)))
+    e2e_ms, h2d, d2h, e2e_steps = measure_e2e(ra, w, q, k, v, flush, max(10, min(args.steps, 30)),
+                                              warmup=max(3, args.warmup))
 
     merge = None if args.no_merge else measure_merge(ra, w, flush, stream)
     others = None
@@ -581,7 +592,8 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
                     "pipelining": "two device buffer sets, three streams: step i's inputs "
                                   "upload while step i-1 computes and step i-2's out/lse "
-                                  "download; the time covers every copy of every step"},
+                                  "download; the time covers every copy of every timed step",
+                    "warmup": max(3, args.warmup)},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms),
