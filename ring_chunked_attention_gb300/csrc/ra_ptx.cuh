@@ -78,6 +78,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// 3-D tiled prefetch of a global tensor box into L2 (no shared memory, no
+// barrier): a later tma_load_3d of the same box finds it in L2.
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // 1-D bulk copy global -> shared, completion counted on an mbarrier (both
 // addresses 16-byte aligned, size a multiple of 16 bytes).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
